@@ -1,0 +1,132 @@
+"""GB300 (sm_103a) exact attention forward: Python binding of ``include/fa.h``.
+
+The binding only marshals arguments; every step of the computation runs in
+the CUDA kernels of ``libfa_gb300.so``.  PyTorch is used for device memory and
+the current stream.  There is no fallback: if the library is missing or the
+device is not sm_103, calls raise.
+
+    o, lse = forward(q, k, v, scale=None, causal=False)
+
+q, k, v: CUDA bf16 tensors [B, H, L, d] (contiguous), d in {64, 128}.
+Returns o (bf16, same shape) and lse (fp32 [B, H, L], natural log).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+from .build import LIB
+
+__all__ = [
+    "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED_D", "FA_ERR_MISALIGNED",
+    "FA_ERR_DEVICE", "FA_ERR_LAUNCH", "FA_ERR_TIMEOUT", "FAError",
+    "library", "fa_fwd", "fa_device_status", "fa_set_wait_timeout_ns", "fa_status_string",
+    "fa_version", "forward", "flops",
+]
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED_D = 2
+FA_ERR_MISALIGNED = 3
+FA_ERR_DEVICE = 4
+FA_ERR_LAUNCH = 5
+FA_ERR_TIMEOUT = 6
+
+
+class FAError(RuntimeError):
+    def __init__(self, code: int, where: str = "fa_fwd"):
+        self.code = code
+        super().__init__(f"{where}: {fa_status_string(code)} (status {code})")
+
+
+_lib = None
+
+
+def library() -> ctypes.CDLL:
+    """The loaded kernel library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            raise RuntimeError(
+                f"{LIB} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'` "
+                "(this package has no CPU or eager fallback)")
+        lib = ctypes.CDLL(LIB)
+        vp, ci = ctypes.c_void_p, ctypes.c_int
+        lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ctypes.c_float, ci, vp]
+        lib.fa_fwd.restype = ci
+        lib.fa_device_status.argtypes = [vp, ci]
+        lib.fa_device_status.restype = ci
+        lib.fa_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+        lib.fa_set_wait_timeout_ns.restype = None
+        lib.fa_status_string.argtypes = [ci]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_version.argtypes = []
+        lib.fa_version.restype = ci
+        _lib = lib
+    return _lib
+
+
+# ---------------------------------------------------------------- raw C ABI
+def fa_fwd(q, k, v, o, lse, B, H, L, d, scale, causal, stream) -> int:
+    """Direct call of the C entry point with integer device addresses."""
+    return library().fa_fwd(q, k, v, o, lse, B, H, L, d, scale, causal, stream)
+
+
+def fa_device_status(stream=None, clear=True) -> int:
+    return library().fa_device_status(stream, int(bool(clear)))
+
+
+def fa_set_wait_timeout_ns(ns: int) -> None:
+    library().fa_set_wait_timeout_ns(int(ns))
+
+
+def fa_status_string(code: int) -> str:
+    return library().fa_status_string(int(code)).decode()
+
+
+def fa_version() -> int:
+    return library().fa_version()
+
+
+# ---------------------------------------------------------------- torch API
+def flops(B, H, L, d, causal) -> float:
+    """Forward FLOPs by the metric's convention: 4*B*H*L^2*d, halved if causal."""
+    f = 4.0 * B * H * L * L * d
+    return f / 2 if causal else f
+
+
+def forward(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
+    """Exact attention forward on CUDA bf16 tensors [B, H, L, d].
+
+    ``scale`` defaults to 1/sqrt(d).  ``out``/``lse`` may be preallocated.
+    Launches asynchronously on ``stream`` (default: torch's current stream).
+    """
+    import torch
+
+    if q.shape != k.shape or q.shape != v.shape or q.dim() != 4:
+        raise ValueError("q, k, v must share one shape [B, H, L, d]")
+    for t in (q, k, v):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous CUDA bfloat16 tensors")
+    B, H, L, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, L), dtype=torch.float32, device=q.device)
+    if out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    if lse.shape != (B, H, L) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B, H, L]")
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                    B, H, L, d, float(scale), int(bool(causal)), stream.cuda_stream)
+    if rc != FA_OK:
+        raise FAError(rc)
+    return out, lse

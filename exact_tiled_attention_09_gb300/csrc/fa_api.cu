@@ -1,0 +1,170 @@
+// Host side of the C ABI declared in include/fa.h: argument validation,
+// tensor-map encoding, kernel selection and launch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_fwd_kernel.cuh"
+
+namespace fa {
+
+__device__ unsigned int g_status;  // wait-site bits; nonzero = a wait gave up
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+unsigned long long g_timeout_ns = 1000000000ull;
+
+// cuTensorMapEncodeTiled, fetched from the driver through the runtime so the
+// library does not link libcuda directly.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// [BH, L, D] bf16 viewed as a 3-D tensor (innermost first: D, L, BH) with a
+// 64 x 128 x 1 box and the 128-byte swizzle.  Rows past L inside a head are
+// out of bounds and read as zeros; they never spill into the next head.
+bool encode_map(CUtensorMap* map, const void* ptr, int BH, int L, int D) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(L) * D * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(BLOCK_N), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, bool CAUSAL>
+int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+           const FwdArgs& args, int BH, cudaStream_t stream, int dev) {
+  auto kernel = fa_fwd_kernel<D, CAUSAL>;
+  constexpr int smem = FwdCfg<D>::SMEM_BYTES;
+  static bool configured[kMaxDevices] = {};
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_DEVICE;
+    if (!configured[dev]) {
+      if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+          cudaSuccess)
+        return FA_ERR_LAUNCH;
+      configured[dev] = true;
+    }
+  }
+  const dim3 grid(static_cast<unsigned>(args.n_qtiles) * static_cast<unsigned>(BH));
+  kernel<<<grid, NUM_THREADS, smem, stream>>>(mq, mk, mv, args);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int L,
+           int d, float scale, int causal, fa_stream_t stream) {
+  using namespace fa;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || L < 1) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  const int64_t n_qt = (static_cast<int64_t>(L) + BLOCK_M - 1) / BLOCK_M;
+  if (BH > 0x7fffffff || BH * n_qt > 0x7fffffff) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4))
+    return FA_ERR_MISALIGNED;
+
+  int dev = -1, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_DEVICE;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return FA_ERR_DEVICE;
+  if (major != 10 || minor != 3) return FA_ERR_DEVICE;
+
+  CUtensorMap mq, mk, mv;
+  if (!encode_map(&mq, q, static_cast<int>(BH), L, d) ||
+      !encode_map(&mk, k, static_cast<int>(BH), L, d) ||
+      !encode_map(&mv, v, static_cast<int>(BH), L, d))
+    return FA_ERR_LAUNCH;
+
+  unsigned int* status = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_status) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+
+  FwdArgs args;
+  args.o = static_cast<uint16_t*>(o);
+  args.lse = lse;
+  args.L = L;
+  args.n_qtiles = static_cast<int>(n_qt);
+  args.scale_log2 = scale * 1.4426950408889634f;
+  args.status = status;
+  args.timeout_ns = g_timeout_ns;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int bh = static_cast<int>(BH);
+  if (d == 64)
+    return causal ? launch<64, true>(mq, mk, mv, args, bh, s, dev)
+                  : launch<64, false>(mq, mk, mv, args, bh, s, dev);
+  return causal ? launch<128, true>(mq, mk, mv, args, bh, s, dev)
+                : launch<128, false>(mq, mk, mv, args, bh, s, dev);
+}
+
+int fa_device_status(fa_stream_t stream, int clear) {
+  using namespace fa;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(v)) != cudaSuccess) return FA_ERR_LAUNCH;
+  if (clear) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_status, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_LAUNCH;
+  }
+  return v ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+void fa_set_wait_timeout_ns(uint64_t ns) { fa::g_timeout_ns = ns < 1000 ? 1000 : ns; }
+
+const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED_D: return "unsupported head dimension (64 or 128)";
+    case FA_ERR_MISALIGNED: return "misaligned pointer (q, k, v, o need 16 bytes; lse 4)";
+    case FA_ERR_DEVICE: return "no usable sm_103 device";
+    case FA_ERR_LAUNCH: return "CUDA launch or runtime error";
+    case FA_ERR_TIMEOUT: return "a kernel wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int fa_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,107 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact attention forward pass.
+ *
+ * The operation is exact scaled-dot-product attention with the per-row
+ * log-sum-exp, computed FlashAttention-style: tiles of Q stay on chip, K and
+ * V stream through in tiles, and an online softmax keeps a running row max
+ * and row sum so the L x L score matrix never reaches global memory.
+ *
+ *   Definition -- "FlashAttention 深度解析" (171host.com), first part,
+ *     section 2.3: S = Q K^T, P = softmax(S), O = P V; scores are scaled
+ *     before the softmax ("FlashAttention: как реально считается attention
+ *     на GPU", section "Формулы online softmax").
+ *   Algorithm -- "04 Transformers, Attention, and FlashAttention", Algorithm 1
+ *     (FlashAttention-2 forward): Q split into row blocks, K/V into column
+ *     blocks; per block the running max m, running sum l and unnormalised O
+ *     are updated; O / l and L = m + log l are written at the end (steps
+ *     12-15).  Causal masking keeps key <= query and skips blocks wholly
+ *     above the diagonal ("FlashAttention 深度解析", second part, section 2.3).
+ *
+ * All entry points are plain C, take raw pointers and sizes, and never
+ * allocate memory.
+ */
+#ifndef FA_GB300_FA_H
+#define FA_GB300_FA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA runtime stream (same type as cudaStream_t); NULL = legacy default. */
+typedef struct CUstream_st *fa_stream_t;
+
+/* Status codes returned by every entry point. */
+enum fa_status {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,   /* null pointer, B/H/L < 1, causal not 0/1,
+                               non-finite scale, or sizes beyond int32 grid /
+                               tensor-map limits                          */
+  FA_ERR_UNSUPPORTED_D = 2, /* head dimension d other than 64 or 128      */
+  FA_ERR_MISALIGNED = 3,    /* q, k, v or o not 16-byte aligned, or lse
+                               not 4-byte aligned                         */
+  FA_ERR_DEVICE = 4,        /* no usable CUDA device, or the current device
+                               is not compute capability 10.3 (sm_103a)   */
+  FA_ERR_LAUNCH = 5,        /* a CUDA runtime call or the launch failed   */
+  FA_ERR_TIMEOUT = 6        /* a kernel's bounded wait gave up (reported by
+                               fa_device_status, never by fa_fwd itself)  */
+};
+
+/*
+ * fa_fwd -- exact attention forward on the current CUDA device.
+ *
+ *   q, k, v : device pointers, bf16, shape [B, H, L, d], row-major and
+ *             contiguous (element (b,h,i,t) at ((b*H + h)*L + i)*d + t);
+ *             16-byte aligned.  Read only.
+ *   o       : device pointer, bf16 [B, H, L, d], same layout; 16-byte
+ *             aligned.  Fully overwritten with
+ *               o[b,h,i,:] = sum_j softmax_j(scale * q_i . k_j) v_j
+ *             over the allowed keys j (all j < L; j <= i when causal),
+ *             rounded to bf16 (nearest even).
+ *   lse     : device pointer, fp32 [B, H, L]; 4-byte aligned.  Fully
+ *             overwritten with log(sum_j exp(scale * q_i . k_j)) over the
+ *             allowed keys (natural log of the scaled scores).
+ *   B, H, L : batch, heads, sequence length (>= 1; queries and keys share L).
+ *   d       : head dimension, 64 or 128.
+ *   scale   : multiplier of q.k before the softmax (finite; 0 and negative
+ *             values are allowed).
+ *   causal  : 0 = every key; 1 = key index <= query index.
+ *   stream  : stream the kernel is launched on.
+ *
+ * The caller owns every buffer; o and lse must not overlap q, k or v.  The
+ * call is asynchronous on `stream`.  On any validation error it returns the
+ * status without launching and without touching o or lse.  Arithmetic: bf16
+ * operands, fp32 accumulation of both products, fp32 softmax statistics.
+ */
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+           int L, int d, float scale, int causal, fa_stream_t stream);
+
+/*
+ * fa_device_status -- synchronise `stream` and report whether any kernel of
+ * this library on the current device gave up a bounded wait since the status
+ * was last cleared (FA_ERR_TIMEOUT) or FA_OK.  A nonzero `clear` resets the
+ * status afterwards.  Returns FA_ERR_LAUNCH if the synchronisation fails.
+ */
+int fa_device_status(fa_stream_t stream, int clear);
+
+/*
+ * fa_set_wait_timeout_ns -- time limit of every wait inside the kernels
+ * (default 1e9 ns).  A wait that exceeds it makes the kernel record
+ * FA_ERR_TIMEOUT, drain its own copies, free its tensor memory and return.
+ * Values below 1000 ns are raised to 1000 ns.  Process-wide; not thread-safe
+ * against concurrent fa_fwd calls.
+ */
+void fa_set_wait_timeout_ns(uint64_t ns);
+
+/* Human-readable text for a status code (static storage, never NULL). */
+const char *fa_status_string(int status);
+
+/* ABI version of this library (major * 10000 + minor * 100 + patch). */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_FA_H */

@@ -1,0 +1,115 @@
+"""The C ABI boundary, on the host: symbols, status strings, validation.
+
+No test here launches a kernel.  Validation errors are returned before any
+CUDA call; the one case with well-formed arguments runs only where no GPU is
+present (it must then report FA_ERR_DEVICE).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_tiled_attention_09_gb300 as fa
+from exact_tiled_attention_09_gb300 import build as kbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return fa.library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(fa_[a-z_0-9]+)\s*\(",
+                                 text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ("fa_fwd", "fa_status_string", "fa_device_status", "fa_set_wait_timeout_ns",
+              "fa_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        s = fa.fa_status_string(code)
+        assert isinstance(s, str) and s
+    assert fa.fa_status_string(0) == "ok"
+    assert fa.fa_status_string(99) == "unknown status"
+    assert fa.fa_version() >= 100
+
+
+GOOD = dict(q=0x10000, k=0x20000, v=0x30000, o=0x40000, lse=0x50000,
+            B=1, H=1, L=128, d=64, scale=0.125, causal=0)
+
+
+def _call(**over):
+    a = dict(GOOD)
+    a.update(over)
+    return fa.fa_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["L"],
+                     a["d"], a["scale"], a["causal"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=0), fa.FA_ERR_INVALID_ARG),
+    (dict(k=0), fa.FA_ERR_INVALID_ARG),
+    (dict(v=0), fa.FA_ERR_INVALID_ARG),
+    (dict(o=0), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=0), fa.FA_ERR_INVALID_ARG),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(H=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(L=0), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=2), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(B=1 << 16, H=1 << 16), fa.FA_ERR_INVALID_ARG),
+    (dict(d=32), fa.FA_ERR_UNSUPPORTED_D),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED_D),
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED_D),
+    (dict(q=0x10008), fa.FA_ERR_MISALIGNED),
+    (dict(o=0x40004), fa.FA_ERR_MISALIGNED),
+    (dict(lse=0x50002), fa.FA_ERR_MISALIGNED),
+])
+def test_validation_errors_launch_nothing(lib, over, code):
+    assert _call(**over) == code
+
+
+def test_well_formed_call_without_gpu_reports_device_error(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; fake pointers must not reach a launch")
+    assert _call() == fa.FA_ERR_DEVICE
+    assert _call(d=128, causal=1) == fa.FA_ERR_DEVICE
+
+
+def test_python_forward_rejects_bad_tensors():
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.forward(q, q, q)  # CPU tensors
+    with pytest.raises(ValueError):
+        fa.forward(q, q[:, :, :4], q)
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "exact_tiled_attention_09_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in src, f
