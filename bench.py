@@ -1,0 +1,427 @@
+"""Benchmark: exact attention forward TFLOPS on GB300 (one JSON line).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one attention forward (the whole hot path, one kernel launch) over
+the headline workload B=4, H=8, L=1024, d=64, non-causal, scale 1/8, inputs
+Q, K, V ~ N(0,1) drawn by the seeded generator and rounded to bf16.  The
+inputs are resident in HBM when timing starts; they fit in L2, so L2 is
+flushed (a 512 MiB write) before every timed step, outside the timed events.
+
+FLOPs per step follow the metric: 4*B*H*L^2*d (halved when causal).
+``value`` = whole-job TFLOP/s = N * FLOPs * K / max over ranks of the summed
+device time of K steps (CUDA events on the launching stream).
+``e2e`` = the same metric through the public call with pinned host buffers:
+every step copies Q, K, V host->device, runs the forward and copies O and
+LSE back, all inside the timed events.
+``roofline`` compares the kernel against the measured dense bf16 peak.
+``cpu_baseline`` times the fp64 oracle on the host cores on the same inputs.
+``workloads`` lists the other synthetic configurations (device-generated
+seeded inputs), each timed the same way, including the d=128 non-causal
+L=8192 point used for the tensor-core fraction.
+
+With more than one GPU (torchrun) every rank runs its own replica of the
+workload (the forward pass has no exchange step); only the timing is
+reduced (max over ranks).
+
+``--impl reference`` times the fp64 CPU oracle instead (rank 0 only): each
+step is one oracle pass over a bounded sample of the headline workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+HEADLINE = "B4_H8_L1024_d64"
+METRIC = "attention fwd TFLOPS (4·B·H·L²·d) and % of GB300 dense BF16 tensor peak"
+FLUSH_BYTES = 512 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------- helpers
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "exact_tiled_attention_09_gb300", "csrc", "*")))
+    for f in files + [os.path.join(ROOT, "include", "fa.h")]:
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this workload,
+    if it was captured on the current kernel source; else None."""
+    src = kernel_source_hash()
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        text = open(path).read()
+        m_w = re.search(r"^workload:\s*(\S+)", text, re.M)
+        m_h = re.search(r"^kernel_source_sha256_16:\s*(\S+)", text, re.M)
+        m_t = re.search(r"^dram_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
+        if m_w and m_h and m_t and m_w.group(1) == workload and m_h.group(1) == src:
+            return float(m_t.group(1)), os.path.relpath(path, ROOT)
+    return None, None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the GPU works."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"fa_bench_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[4:9], float(parts[3])))
+            except ValueError:
+                continue
+        os.remove(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm_max = max(r[1] for r in rows)
+        loaded = [r for r in rows if r[3] > 200.0] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i in range(4)
+                          if r[2][1 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": sm_max,
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": max(r[3] for r in rows)}
+
+
+# ----------------------------------------------------------------- CPU leg
+def oracle_sample_run(w, qb, kb, vb, heads, threads=0):
+    """One oracle pass over ``heads`` whole heads of the workload; returns
+    (seconds, flops)."""
+    import numpy as np
+
+    import oracle
+    from fa_inputs import bf16_bits_to_float32
+
+    BH = w.B * w.H
+    f = lambda b: bf16_bits_to_float32(b.reshape(BH, w.L, w.d)[:heads]).astype(np.float64)
+    q, k, v = f(qb), f(kb), f(vb)
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, w.scale, w.causal, threads=threads)
+    dt = time.perf_counter() - t0
+    return dt, w.flops * heads / BH
+
+
+def cpu_baseline(w, qb, kb, vb, target_s=6.0):
+    """Oracle TFLOP/s on the host cores, on a bounded sample of the workload."""
+    BH = w.B * w.H
+    dt, fl = oracle_sample_run(w, qb, kb, vb, 1)
+    heads = max(1, min(BH, int(target_s / max(dt, 1e-3))))
+    reps = 1
+    if heads == BH:
+        dt, fl = oracle_sample_run(w, qb, kb, vb, BH)
+        reps = max(1, int(target_s / max(dt, 1e-3)))
+    total_t, total_f = 0.0, 0.0
+    for _ in range(reps):
+        dt, fl = oracle_sample_run(w, qb, kb, vb, heads)
+        total_t += dt
+        total_f += fl
+    cores = os.cpu_count() or 1
+    return {"value": total_f / total_t / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{heads} of {BH} heads of {w.name}, x{reps}, fp64, {total_t:.1f} s wall"}
+
+
+# ----------------------------------------------------------------- GPU leg
+def device_inputs(w, dev, torch):
+    """Seeded normal inputs generated on the device (for the extra workloads)."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    shape = (w.B, w.H, w.L, w.d)
+    mk = lambda s: (torch.randn(shape, generator=g, device=dev, dtype=torch.float32) * s).to(
+        torch.bfloat16)
+    return mk(w.q_std), mk(w.k_std), mk(w.v_std)
+
+
+def time_forward(fa, torch, q, k, v, w, steps, warmup, flush_buf, o=None, lse=None):
+    """Per-step device time (ms) of ``fa.forward``; L2 flushed before each step."""
+    stream = torch.cuda.current_stream()
+    if o is None:
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.L), dtype=torch.float32, device=q.device)
+    for _ in range(warmup):
+        fa.forward(q, k, v, scale=w.scale, causal=w.causal, out=o, lse=lse, stream=stream)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for s, e in ev:
+        flush_buf.fill_(1)
+        s.record(stream)
+        fa.forward(q, k, v, scale=w.scale, causal=w.causal, out=o, lse=lse, stream=stream)
+        e.record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in ev]
+
+
+def time_e2e(fa, torch, host, w, steps, warmup, flush_buf, dev):
+    """Per-step time (ms) of H2D(Q,K,V) + forward + D2H(O, LSE) from pinned memory."""
+    qh, kh, vh = host
+    qd, kd, vd = (torch.empty_like(x, device=dev) for x in host)
+    od = torch.empty_like(qd)
+    ld = torch.empty((w.B, w.H, w.L), dtype=torch.float32, device=dev)
+    oh = torch.empty_like(qh).pin_memory()
+    lh = torch.empty((w.B, w.H, w.L), dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream()
+
+    def step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        fa.forward(qd, kd, vd, scale=w.scale, causal=w.causal, out=od, lse=ld, stream=stream)
+        oh.copy_(od, non_blocking=True)
+        lh.copy_(ld, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for s, e in ev:
+        flush_buf.fill_(1)
+        s.record(stream)
+        step()
+        e.record(stream)
+    torch.cuda.synchronize()
+    h2d = sum(x.numel() * x.element_size() for x in host)
+    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+    return [s.elapsed_time(e) for s, e in ev], h2d, d2h
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import exact_tiled_attention_09_gb300 as fa
+    from fa_inputs import WORKLOADS, make_qkv
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fa.library()
+    peaks, peak_src = read_peaks()
+
+    w = WORKLOADS[args.workload]
+    if args.device_inputs:
+        q, k, v = device_inputs(w, dev, torch)
+        host = tuple(x.cpu().pin_memory() for x in (q, k, v))
+    else:
+        qb, kb, vb = make_qkv(w)
+        as_t = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16)
+        host = tuple(as_t(x).pin_memory() for x in (qb, kb, vb))
+        q, k, v = (x.to(dev) for x in host)
+    flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    # CPU baseline first (before the GPU clocks are sampled), rank 0 only
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline and not args.device_inputs:
+        cpu = cpu_baseline(w, qb, kb, vb)
+
+    extras = []
+    with ClockSampler(local) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ms = time_forward(fa, torch, q, k, v, w, args.steps, args.warmup, flush_buf)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e2e_ms, h2d, d2h = time_e2e(fa, torch, host, w, args.steps, args.warmup, flush_buf, dev)
+        if rank == 0 and not args.no_extra:
+            for name, wx in WORKLOADS.items():
+                if name == w.name:
+                    continue
+                qx, kx, vx = device_inputs(wx, dev, torch)
+                steps = max(3, min(args.extra_steps, int(2e13 / wx.flops)))
+                t = time_forward(fa, torch, qx, kx, vx, wx, steps, 3, flush_buf)
+                mean = sum(t) / len(t)
+                tf = wx.flops / (mean * 1e-3) / 1e12
+                extras.append({"workload": name, "B": wx.B, "H": wx.H, "L": wx.L, "d": wx.d,
+                               "causal": wx.causal, "ms_mean": round(mean, 4),
+                               "ms_min": round(min(t), 4), "tflops": round(tf, 1),
+                               "frac_of_peak": round(tf / peaks["bf16_tflops"], 4),
+                               "steps": steps})
+                del qx, kx, vx
+    if fa.fa_device_status(None, clear=True) != fa.FA_OK:
+        raise RuntimeError("a kernel wait timed out during the benchmark")
+
+    total_ms = sum(ms)
+    total_e2e = sum(e2e_ms)
+    if world > 1:
+        t = torch.tensor([total_ms, total_e2e], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, total_e2e = float(t[0]), float(t[1])
+    flops_step = w.flops
+    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    e2e_value = world * flops_step * args.steps / (total_e2e * 1e-3) / 1e12
+    mean_launch_ms = sum(ms) / len(ms)
+    achieved = flops_step / (mean_launch_ms * 1e-3) / 1e12
+    traffic, traffic_src = read_traffic(w.name)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "TFLOP/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(total_ms / args.steps, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded SplitMix64 + Box-Muller normals rounded to bf16)",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d,
+                       "causal": w.causal, "scale": w.scale,
+                       "l2": "flushed before every timed step (512 MiB device write, untimed)",
+                       "parallelism": f"replicas x{world} (no exchange step)"},
+            "percent_of_peak": round(100 * value / world / peaks["bf16_tflops"], 2),
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
+                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": round(achieved / peaks["bf16_tflops"], 4),
+                         "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed alone)",
+                         "traffic": traffic, "traffic_source": traffic_src,
+                         "algorithmic_bytes": w.algorithmic_bytes,
+                         "kernel": f"fa_fwd_kernel<{w.d},{str(w.causal).lower()}>",
+                         "ms_mean": round(mean_launch_ms, 5), "ms_min": round(min(ms), 5)},
+            "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": round(total_e2e / args.steps, 5)},
+            "gpu_launches": args.steps,
+            "clocks": clk.summary(),
+            "cpu_baseline": cpu,
+            "workloads": extras,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The fp64 oracle on the host cores, same metric/config (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    from fa_inputs import WORKLOADS, make_qkv
+
+    w = WORKLOADS[args.workload]
+    qb, kb, vb = make_qkv(w)
+    BH = w.B * w.H
+    # bounded sample per step: whole heads, about one second of host work
+    dt, _ = oracle_sample_run(w, qb, kb, vb, 1)
+    heads = max(1, min(BH, int(1.0 / max(dt, 1e-3))))
+    for _ in range(args.warmup):
+        oracle_sample_run(w, qb, kb, vb, heads)
+    total_t, total_f = 0.0, 0.0
+    for _ in range(args.steps):
+        t, f = oracle_sample_run(w, qb, kb, vb, heads)
+        total_t += t
+        total_f += f
+    value = total_f / total_t / 1e12
+    cores = os.cpu_count() or 1
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total_t / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded SplitMix64 + Box-Muller normals rounded to bf16)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d,
+                   "causal": w.causal, "scale": w.scale},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{heads} of {BH} heads of {w.name} per step, fp64"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--extra-steps", type=int, default=30)
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--device-inputs", action="store_true",
+                    help="draw the headline inputs with a seeded device generator "
+                         "(no CPU baseline then); used for profiling large workloads")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
