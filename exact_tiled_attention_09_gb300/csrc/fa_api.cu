@@ -75,7 +75,7 @@ int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
       configured[dev] = true;
     }
   }
-  const dim3 grid(static_cast<unsigned>(args.n_qtiles) * static_cast<unsigned>(BH));
+  const dim3 grid(static_cast<unsigned>(args.n_ctiles) * static_cast<unsigned>(BH));
   kernel<<<grid, NUM_THREADS, smem, stream>>>(mq, mk, mv, args);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
@@ -96,8 +96,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
   const int64_t BH = static_cast<int64_t>(B) * H;
-  const int64_t n_qt = (static_cast<int64_t>(L) + BLOCK_M - 1) / BLOCK_M;
-  if (BH > 0x7fffffff || BH * n_qt > 0x7fffffff) return FA_ERR_INVALID_ARG;
+  const int64_t n_ct = (static_cast<int64_t>(L) + ROWS_PER_CTA - 1) / ROWS_PER_CTA;
+  if (BH > 0x7fffffff || BH * n_ct > 0x7fffffff) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
       !aligned(lse, 4))
     return FA_ERR_MISALIGNED;
@@ -123,7 +123,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   args.o = static_cast<uint16_t*>(o);
   args.lse = lse;
   args.L = L;
-  args.n_qtiles = static_cast<int>(n_qt);
+  args.n_ctiles = static_cast<int>(n_ct);
   args.scale_log2 = scale * 1.4426950408889634f;
   args.status = status;
   args.timeout_ns = g_timeout_ns;

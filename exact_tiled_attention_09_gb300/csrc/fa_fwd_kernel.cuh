@@ -1,36 +1,48 @@
 // Exact attention forward for sm_103a: TMA + tcgen05 + TMEM, online softmax.
 //
-// One CTA owns one tile of BLOCK_M = 128 query rows of one (batch, head) and
-// walks the K/V blocks of BLOCK_N = 128 keys in order, as in the
+// Work unit: one CTA owns 2 x 128 query rows (two Q tiles) of one
+// (batch, head) and walks the K/V blocks of 128 keys in order, as in the
 // FlashAttention-2 forward ("04 Transformers, Attention, and FlashAttention",
 // Algorithm 1: Q split into row blocks, the K/V loop inside, running max m,
-// running sum l and unnormalised O on chip, O / l and m + log l at the end).
+// running sum l and unnormalised O kept on chip, O / l and m + log l written
+// at the end).  Two Q tiles per CTA let the tensor core work on one tile
+// while the softmax of the other runs (the overlap of matmul and softmax that
+// "FlashAttention 深度解析", third part, section 2.2 describes for Hopper,
+// re-targeted here to tcgen05 and tensor memory).
 //
-// Warp roles (192 threads):
-//   warp 0      TMA producer: loads Q once, then streams K_j and V_j tiles
-//               through a ring of shared-memory slots (full/empty mbarriers).
-//   warp 1      MMA issuer (one thread): S_j = Q K_j^T into a TMEM buffer
-//               (two buffers, so S_{j+1} is computed while the softmax works
-//               on S_j), then O += P_j V_j with P_j read from TMEM.  The
-//               whole warp allocates and frees the tensor memory.
-//   warps 2..5  softmax: thread r owns query row r (TMEM lane r).  Per block
-//               it reads its 128 scores, applies the masks, updates the
-//               running max, writes P = exp2(scale*log2e*S - m) as bf16 over
-//               the scores it came from, and rescales O (and l) by
-//               exp2(m_old - m_new) whenever the running max grew; a warp
-//               skips the O pass when no row in it saw a larger max (the
-//               correction is then exactly 1).  At the end it writes O / l
-//               (bf16) and the log-sum-exp (fp32).
+// Warp roles (320 threads):
+//   warp 0      MMA issuer (one thread) and owner of the tensor memory
+//   warp 1      TMA producer: loads Q0 and Q1 once, then K_j and V_j tiles
+//               into a ring of shared-memory slots (full/empty mbarriers)
+//   warps 2..5  softmax of Q tile 0 (row r = TMEM lane r; warp w may only
+//               touch lanes 32*(w%4) .. 32*(w%4)+31, so the four warps of a
+//               group cover quarters 2, 3, 0, 1)
+//   warps 6..9  softmax of Q tile 1
+// The MMA warp has the lowest warp index on its scheduler: when its single
+// thread is ready to issue it is not held back behind the softmax warps.
 //
-// Tensor memory (512 columns x 128 lanes, fp32):
-//   [0,128)    S buffer 0 (P_j packed bf16 in its first 64 columns)
-//   [128,256)  S buffer 1
-//   [256,256+D) O accumulator
+// MMA order per K/V block j (each S_t buffer holds P_t after the softmax, so
+// S_t of block j+1 is issued only after O_t += P_t V_j of block j):
+//   PV0_j, S0_{j+1}, PV1_j, S1_{j+1}
+// The tensor core therefore computes PV1_j and S1_{j+1} while softmax 0
+// works on S0_{j+1}, and the other way round.  Because tcgen05 operations of
+// one thread complete in issue order, the arrival that publishes S_t of
+// block j+1 also proves O_t += P_t V_j finished, so the softmax may rescale
+// O_t right away.
 //
-// Shared memory (1024-byte aligned): NSLOT ring slots of one 128 x D tile
-// each, then the Q tile, then the mbarriers.  A tile is stored as D/64
-// boxes of 128 rows x 64 columns with the 128-byte swizzle, the layout the
-// tensor map writes and the MMA descriptors read.
+// Softmax per block (per row): scores s -> mask -> m_new = max(m, rowmax)
+// (in units of scale*log2(e)) -> P~ = exp2(s*scale*log2e - m_new) written as
+// bf16 over the first 64 columns of its S buffer -> l = c*l + rowsum(P~) and
+// O *= c with c = exp2(m - m_new) whenever the max grew (a warp skips the O
+// pass when no row of it changed: c is then exactly 1).
+//
+// Tensor memory (512 columns x 128 lanes of 32 bits):
+//   [0,128) S0/P0   [128,256) S1/P1   [256,256+D) O0   [256+D,256+2D) O1
+//
+// Shared memory (1024-byte aligned): NSLOT ring slots, then Q0 and Q1, then
+// the mbarriers.  Every tile is stored as D/64 boxes of 128 rows x 64 columns
+// with the 128-byte swizzle, the layout the tensor map writes and the MMA
+// descriptors read.
 #pragma once
 
 #include <cuda.h>
@@ -42,18 +54,15 @@
 
 namespace fa {
 
-constexpr int BLOCK_M = 128;
-constexpr int BLOCK_N = 128;
-constexpr int NUM_THREADS = 192;
-// Rescale threshold (log2 units).  Zero keeps the exact running max of the
-// recurrence, so the largest P~ of a row is exp2(0) = 1, exact in bf16.  A
-// positive threshold (keeping a stale max while it is within TAU) saves
-// rescale passes but rounds the dominant weight of peaked rows to bf16,
-// which costs up to 2^-9 relative on O.
-constexpr float RESCALE_TAU = 0.0f;
+constexpr int BLOCK_M = 128;          // rows per Q tile (one TMEM lane each)
+constexpr int BLOCK_N = 128;          // keys per K/V block
+constexpr int TILES_PER_CTA = 2;
+constexpr int ROWS_PER_CTA = BLOCK_M * TILES_PER_CTA;
+constexpr int NUM_THREADS = 320;
+constexpr int MMA_WARP = 0;
+constexpr int PRODUCER_WARP = 1;
+constexpr int FIRST_SOFTMAX_WARP = 2;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t S_COL = 0;        // buffer b at S_COL + 128 * b
-constexpr uint32_t O_COL = 256;
 constexpr int BOX_BYTES = 128 * 64 * 2;  // one 128-row x 64-column bf16 box
 
 // Wait sites (bit index in the device status word).
@@ -72,21 +81,25 @@ struct FwdCfg {
   static_assert(D == 64 || D == 128, "head dimension must be 64 or 128");
   static constexpr int BOXES = D / 64;
   static constexpr int TILE_BYTES = BLOCK_N * D * 2;
-  static constexpr int NSLOT = (D == 64) ? 8 : 5;
+  static constexpr int NSLOT = (D == 64) ? 8 : 4;
   static constexpr int Q_OFF = NSLOT * TILE_BYTES;
-  static constexpr int BAR_OFF = Q_OFF + TILE_BYTES;
-  // q_full, full[NSLOT], empty[NSLOT], s_full[2], p_full[2], o_ready, drain
-  static constexpr int NBAR = 1 + 2 * NSLOT + 2 + 2 + 1 + 1;
+  static constexpr int BAR_OFF = Q_OFF + TILES_PER_CTA * TILE_BYTES;
+  // q_full, full[NSLOT], empty[NSLOT], s_full[2], p_full[2], o_done[2], drain
+  static constexpr int NBAR = 1 + 2 * NSLOT + 2 + 2 + 2 + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + alignment slack
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  __host__ __device__ static constexpr uint32_t S_COL(int t) { return 128u * t; }
+  __host__ __device__ static constexpr uint32_t O_COL(int t) {
+    return 256u + static_cast<uint32_t>(D) * t;
+  }
 };
 
 struct FwdArgs {
   uint16_t* o;        // bf16 [BH, L, D]
   float* lse;         // fp32 [BH, L]
   int L;
-  int n_qtiles;       // ceil(L / BLOCK_M)
+  int n_ctiles;       // ceil(L / ROWS_PER_CTA)
   float scale_log2;   // scale * log2(e)
   unsigned int* status;
   unsigned long long timeout_ns;
@@ -102,6 +115,16 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity,
   }
 }
 
+// Number of K/V blocks Q tile t of this CTA needs (0 if the tile lies wholly
+// past the end of the sequence).  Causal: blocks whose first key exceeds the
+// tile's last query are skipped.
+template <bool CAUSAL>
+__device__ __forceinline__ int blocks_for_tile(int row0, int L) {
+  if (row0 >= L) return 0;
+  const int all = (L + BLOCK_N - 1) / BLOCK_N;
+  return CAUSAL ? min(all, (row0 + BLOCK_M - 1) / BLOCK_N + 1) : all;
+}
+
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -113,31 +136,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* const base_ptr = smem_raw + (base - raw);
 
   const uint32_t ring = base;
-  const uint32_t sQ = base + C::Q_OFF;
+  const uint32_t sQ = base + C::Q_OFF;  // tile t at sQ + t * TILE_BYTES
   const uint32_t bars = base + C::BAR_OFF;
   const uint32_t bar_q = bars;
   auto bar_full = [&](int s) { return bars + 8u * (1 + s); };
   auto bar_empty = [&](int s) { return bars + 8u * (1 + C::NSLOT + s); };
-  auto bar_s = [&](int b) { return bars + 8u * (1 + 2 * C::NSLOT + b); };
-  auto bar_p = [&](int b) { return bars + 8u * (3 + 2 * C::NSLOT + b); };
-  const uint32_t bar_o = bars + 8u * (5 + 2 * C::NSLOT);
-  const uint32_t bar_drain = bars + 8u * (6 + 2 * C::NSLOT);
+  auto bar_s = [&](int t) { return bars + 8u * (1 + 2 * C::NSLOT + t); };
+  auto bar_p = [&](int t) { return bars + 8u * (3 + 2 * C::NSLOT + t); };
+  auto bar_o = [&](int t) { return bars + 8u * (5 + 2 * C::NSLOT + t); };
+  const uint32_t bar_drain = bars + 8u * (7 + 2 * C::NSLOT);
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + C::MISC_OFF);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::MISC_OFF + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int L = args.L;
-  const int n_qt = args.n_qtiles;
+  const int n_ct = args.n_ctiles;
 
-  // Tile order: head-major, so the CTAs resident at one time share the K/V
-  // of a few heads in L2.  Causal: heaviest (last) query tile of a head first.
-  const int bh = static_cast<int>(blockIdx.x) / n_qt;
-  const int qt_raw = static_cast<int>(blockIdx.x) % n_qt;
-  const int qt = CAUSAL ? (n_qt - 1 - qt_raw) : qt_raw;
-  const int n_kv_all = (L + BLOCK_N - 1) / BLOCK_N;
-  // Causal: blocks wholly above the diagonal (first key > last query) skipped.
-  const int n_kv = CAUSAL ? min(n_kv_all, (qt * BLOCK_M + BLOCK_M - 1) / BLOCK_N + 1) : n_kv_all;
+  // CTA order: head-major, so the CTAs resident at one time share the K/V of
+  // a few heads in L2.  Causal: the heaviest (last) rows of a head first.
+  const int bh = static_cast<int>(blockIdx.x) / n_ct;
+  const int ct_raw = static_cast<int>(blockIdx.x) % n_ct;
+  const int ct = CAUSAL ? (n_ct - 1 - ct_raw) : ct_raw;
+  const int row_base = ct * ROWS_PER_CTA;
+  const int n_blk0 = blocks_for_tile<CAUSAL>(row_base, L);
+  const int n_blk1 = blocks_for_tile<CAUSAL>(row_base + BLOCK_M, L);
+  const int n_blk = max(n_blk0, n_blk1);  // K/V blocks loaded
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
@@ -145,21 +169,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(bar_full(s), 1);
       mbar_init(bar_empty(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar_s(b), 1);
-      mbar_init(bar_p(b), 4 * 32);
+    for (int t = 0; t < TILES_PER_CTA; ++t) {
+      mbar_init(bar_s(t), 1);
+      mbar_init(bar_p(t), 4);  // one arrival per softmax warp
+      mbar_init(bar_o(t), 1);
     }
-    mbar_init(bar_o, 1);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
-  if (warp == 0 && lane == 0) {
+  if (warp == PRODUCER_WARP && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
-  if (warp == 1) {
+  if (warp == MMA_WARP) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tmem_relinquish();
   }
@@ -169,12 +193,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, args.status, args.timeout_ns};
 
-  if (warp == 0) {
+  if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar_q, C::TILE_BYTES);
-      for (int c = 0; c < C::BOXES; ++c)
-        tma_load_3d(sQ + c * BOX_BYTES, &tmQ, bar_q, c * 64, qt * BLOCK_M, bh);
+      mbar_arrive_expect_tx(bar_q, TILES_PER_CTA * C::TILE_BYTES);
+      for (int t = 0; t < TILES_PER_CTA; ++t)
+        for (int c = 0; c < C::BOXES; ++c)
+          tma_load_3d(sQ + t * C::TILE_BYTES + c * BOX_BYTES, &tmQ, bar_q, c * 64,
+                      row_base + t * BLOCK_M, bh);
       int cnt = 0;
       bool ok = true;
       auto load = [&](const CUtensorMap* map, int j) -> bool {
@@ -188,12 +214,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ++cnt;
         return true;
       };
-      // Same order the MMA warp consumes: K_0, K_1, V_0, K_2, V_1, ..., V_last.
-      for (int j = 0; j < n_kv && ok; ++j) {
+      // Ring positions: K_j at 2j, V_j at 2j + 1 (the MMA warp's first uses
+      // come in this order).
+      for (int j = 0; j < n_blk && ok; ++j) {
         ok = load(&tmK, j);
-        if (ok && j > 0) ok = load(&tmV, j - 1);
+        if (ok) ok = load(&tmV, j);
       }
-      if (ok) ok = load(&tmV, n_kv - 1);
       if (!ok) {
         // Let every copy already issued land before the CTA exits.
         mbar_wait_drain(bar_q, 0, args.timeout_ns);
@@ -203,59 +229,74 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t IDESC_S = idesc_bf16_f32(BLOCK_M, BLOCK_N, false);
       constexpr uint32_t IDESC_O = idesc_bf16_f32(BLOCK_M, D, true);
-      int cnt = 0;
+      auto n_t = [&](int t) { return t == 0 ? n_blk0 : n_blk1; };
       bool ok = mbar_wait(bar_q, 0, ctl, SITE_Q);
       tc_fence_after();
-      auto take = [&](uint32_t& addr, int& s) -> bool {
-        s = cnt % C::NSLOT;
-        const uint32_t use = static_cast<uint32_t>(cnt / C::NSLOT);
+      // Wait for ring position `pos` to be filled; returns its slot address.
+      auto acquire = [&](int pos, uint32_t& addr) -> bool {
+        const int s = pos % C::NSLOT;
+        const uint32_t use = static_cast<uint32_t>(pos / C::NSLOT);
         if (!mbar_wait(bar_full(s), use & 1u, ctl, SITE_FULL)) return false;
         tc_fence_after();
         addr = ring + s * C::TILE_BYTES;
-        ++cnt;
         return true;
       };
-      auto issue_s = [&](int j) -> bool {
-        uint32_t kaddr;
-        int s;
-        if (!take(kaddr, s)) return false;
-        const uint32_t d_tmem = tmem + S_COL + 128u * (j & 1);
+      auto release = [&](int pos) { mma_commit(bar_empty(pos % C::NSLOT)); };
+      auto issue_s = [&](int t, uint32_t kaddr) {
+        const uint32_t q = sQ + t * C::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
-          mma_ss(d_tmem, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kaddr + off, 16, 1024),
-                 IDESC_S, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + C::S_COL(t), sdesc_sw128(q + off, 16, 1024),
+                 sdesc_sw128(kaddr + off, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar_empty(s));
-        mma_commit(bar_s(j & 1));
-        return true;
+        mma_commit(bar_s(t));
       };
-      auto issue_pv = [&](int j) -> bool {
-        if (!mbar_wait(bar_p(j & 1), (j >> 1) & 1, ctl, SITE_P)) return false;
+      auto issue_pv = [&](int t, int j, uint32_t vaddr) -> bool {
+        if (!mbar_wait(bar_p(t), j & 1, ctl, SITE_P)) return false;
         tc_fence_after();
-        uint32_t vaddr;
-        int s;
-        if (!take(vaddr, s)) return false;
-        const uint32_t p_tmem = tmem + S_COL + 128u * (j & 1);
 #pragma unroll
         for (int kk = 0; kk < BLOCK_N / 16; ++kk) {
-          mma_ts(tmem + O_COL, p_tmem + kk * 8, sdesc_sw128(vaddr + kk * 2048, BOX_BYTES, 1024),
-                 IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + kk * 8,
+                 sdesc_sw128(vaddr + kk * 2048, BOX_BYTES, 1024), IDESC_O,
+                 (j > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(bar_empty(s));
-        mma_commit(bar_o);
+        if (j == n_t(t) - 1) mma_commit(bar_o(t));
         return true;
       };
-      for (int j = 0; j < n_kv && ok; ++j) {
-        ok = issue_s(j);
-        if (ok && j > 0) ok = issue_pv(j - 1);
+
+      uint32_t kaddr = 0, vaddr = 0;
+      if (ok && n_blk > 0) {
+        ok = acquire(0, kaddr);
+        if (ok) {
+          for (int t = 0; t < TILES_PER_CTA; ++t)
+            if (n_t(t) > 0) issue_s(t, kaddr);
+          release(0);
+        }
       }
-      if (ok) ok = issue_pv(n_kv - 1);
+      for (int j = 0; j < n_blk && ok; ++j) {
+        ok = acquire(2 * j + 1, vaddr);
+        // K_{j+1} is taken just before its first use, so PV0_j never waits
+        // for it.  Some tile uses K_{j+1} whenever j + 1 < n_blk.
+        bool k_next = false;
+        for (int t = 0; t < TILES_PER_CTA && ok; ++t) {
+          if (j < n_t(t)) ok = issue_pv(t, j, vaddr);
+          if (ok && j + 1 < n_t(t)) {
+            if (!k_next) ok = acquire(2 * j + 2, kaddr);
+            k_next = true;
+            if (ok) issue_s(t, kaddr);
+          }
+        }
+        if (ok) {
+          release(2 * j + 1);
+          if (k_next) release(2 * j + 2);
+        }
+      }
       if (!ok) {
         // Every MMA already issued must finish before the tensor memory is freed.
         mma_commit(bar_drain);
@@ -264,19 +305,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int t = (warp - FIRST_SOFTMAX_WARP) >> 2;  // Q tile of this warpgroup
+    const int quarter = warp & 3;     // TMEM lanes this warp may access
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const int q_row = qt * BLOCK_M + row;
+    const uint32_t s_col = C::S_COL(t);
+    const uint32_t o_col = C::O_COL(t);
+    const int tile_row0 = row_base + t * BLOCK_M;
+    const int q_row = tile_row0 + row;
+    const int n_my = t == 0 ? n_blk0 : n_blk1;
     const float sl2 = args.scale_log2;
     const bool pos_scale = sl2 > 0.f;
-    float m = -INFINITY;  // running max of scale*log2e*s (or the stale reference)
-    float l = 0.f;        // running sum of P~ in that reference
+    float m = -INFINITY;  // running max of scale*log2e*s
+    float l = 0.f;        // running sum of P~ relative to m
     bool ok = true;
 
-    for (int j = 0; j < n_kv; ++j) {
-      const int b = j & 1;
-      const bool w = mbar_wait(bar_s(b), (j >> 1) & 1, ctl, SITE_S);
+    for (int j = 0; j < n_my; ++j) {
+      const bool w = mbar_wait(bar_s(t), j & 1, ctl, SITE_S);
       if (!__all_sync(0xffffffffu, w)) {
         ok = false;
         break;
@@ -284,14 +329,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       uint32_t sr[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + S_COL + 128u * b + 32u * c, sr[c]);
+      for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + s_col + 32u * c, sr[c]);
       tmem_wait_ld();
 #pragma unroll
       for (int c = 0; c < 4; ++c) reg_fence32(sr[c]);
 
       // Masks: keys past the end of the sequence; causal keys after the query.
       const int k0 = j * BLOCK_N;
-      const bool need_mask = (k0 + BLOCK_N > L) || (CAUSAL && k0 + BLOCK_N - 1 > qt * BLOCK_M);
+      const bool need_mask = (k0 + BLOCK_N > L) || (CAUSAL && k0 + BLOCK_N - 1 > tile_row0);
       if (need_mask) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -303,17 +348,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
       }
 
-      // Row max in scaled log2 units.
-      float mx[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) mx[t] = -INFINITY;
+      // Row max in units of scale*log2(e).
+      float blk;
       if (pos_scale) {
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(sr[c][e]));
+          for (int e = 0; e < 32; e += 8) {
+            mx[0] = fmax3(mx[0], __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+            mx[1] = fmax3(mx[1], __uint_as_float(sr[c][e + 2]), __uint_as_float(sr[c][e + 3]));
+            mx[2] = fmax3(mx[2], __uint_as_float(sr[c][e + 4]), __uint_as_float(sr[c][e + 5]));
+            mx[3] = fmax3(mx[3], __uint_as_float(sr[c][e + 6]), __uint_as_float(sr[c][e + 7]));
+          }
+        blk = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]) * sl2;
       } else {
         // scale <= 0: work on x = scale*log2e*s directly (masked stays -inf).
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -321,74 +372,83 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const float s = __uint_as_float(sr[c][e]);
             const float x = (s == -INFINITY) ? -INFINITY : s * sl2;
             sr[c][e] = __float_as_uint(x);
-            mx[e & 7] = fmaxf(mx[e & 7], x);
+            mx[e & 3] = fmaxf(mx[e & 3], x);
           }
+        blk = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
       }
-      float blk = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                        fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      if (pos_scale) blk *= sl2;
       const float m_new = fmaxf(m, blk);
-
+      // Every row sees at least one unmasked key in every block it visits,
+      // so m_new is finite here.
       float corr = 1.f;
-      bool rescale = false;
-      if (j == 0) {
-        m = m_new;
-      } else if (m_new - m > RESCALE_TAU) {
-        corr = ex2_approx(m - m_new);
-        m = m_new;
-        rescale = true;
-      }
-      // P~ = exp2(x - m); x = s*sl2 (fused) or the precomputed x.
+      const bool grew = j > 0 && m_new > m;
+      if (grew) corr = ex2_approx(m - m_new);
+      m = m_new;
+
+      // P~ = exp2(x - m) with x = s*sl2 (fused, two lanes per instruction) or
+      // the precomputed x; the row sum accumulates in four packed pairs.
       const float mul = pos_scale ? sl2 : 1.f;
-      const float neg_m = -m;
-      float sum[8];
+      const uint64_t mul2 = f2_pack(mul, mul);
+      const uint64_t negm2 = f2_pack(-m, -m);
+      uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
+      // Keys 32c..32c+31 pack into columns 16c..16c+15 of the S buffer.
 #pragma unroll
-      for (int t = 0; t < 8; ++t) sum[t] = 0.f;
-      uint32_t pk[2][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][e]), mul, neg_m));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][e + 1]), mul, neg_m));
-          sum[e & 7] += p0;
-          sum[(e + 1) & 7] += p1;
-          const int col = c * 32 + e;  // key within the block
-          pk[col >> 6][(col & 63) >> 1] = pack_bf16x2(p0, p1);
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])), mul2,
+                           negm2),
+                    x0, x1);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          sum2[(e >> 1) & 3] = f2_add(sum2[(e >> 1) & 3], f2_pack(p0, p1));
+          pk[e >> 1] = pack_bf16x2(p0, p1);
         }
-      tmem_st32(lane_base + S_COL + 128u * b, pk[0]);
-      tmem_st32(lane_base + S_COL + 128u * b + 32u, pk[1]);
-      const float rowsum =
-          ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
+        tmem_st16(lane_base + s_col + 16u * c, pk);
+      }
+      float s_lo, s_hi;
+      f2_unpack(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), s_lo, s_hi);
+      const float rowsum = s_lo + s_hi;
       l = (j == 0) ? rowsum : fmaf(corr, l, rowsum);
 
-      if (__any_sync(0xffffffffu, rescale)) {
-        // O holds P_0..P_{j-1} contributions once PV_{j-1} (the j-th commit) is done.
-        const bool wo = mbar_wait(bar_o, (j - 1) & 1, ctl, SITE_O);
-        if (!__all_sync(0xffffffffu, wo)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+      // O_t is quiescent here: the arrival on s_full for this block came
+      // after O_t += P_t V_{j-1} completed, and the next PV waits for p_full.
+      if (__any_sync(0xffffffffu, grew)) {
+        // All of O_t's columns in one round trip: issue every load, wait
+        // once, scale in packed pairs, store back.
+        uint32_t ov[D / 32][32];
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_base + o_col + 32u * c, ov[c]);
+        tmem_wait_ld();
+        const uint64_t corr2 = f2_pack(corr, corr);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(lane_base + O_COL + 32u * c, ov);
-          tmem_wait_ld();
-          reg_fence32(ov);
+          reg_fence32(ov[c]);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * corr);
-          tmem_st32(lane_base + O_COL + 32u * c, ov);
+          for (int e = 0; e < 32; e += 2) {
+            float a, b;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(ov[c][e]), __uint_as_float(ov[c][e + 1])),
+                             corr2),
+                      a, b);
+            ov[c][e] = __float_as_uint(a);
+            ov[c][e + 1] = __float_as_uint(b);
+          }
+          tmem_st32(lane_base + o_col + 32u * c, ov[c]);
         }
       }
+      // One arrival per warp: every lane's tensor-memory stores are complete
+      // (wait::st) and ordered (fence) before the warp syncs and lane 0
+      // arrives.  128 separate arrivals on one barrier word serialise.
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar_p(b));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_p(t));
     }
 
-    if (ok) {
-      // Epilogue: wait for the last PV (commit number n_kv), then O / l and LSE.
-      const bool w = mbar_wait(bar_o, (n_kv - 1) & 1, ctl, SITE_O);
+    if (ok && n_my > 0) {
+      // Epilogue: wait for the last O_t += P_t V, then O / l and LSE.
+      const bool w = mbar_wait(bar_o(t), 0, ctl, SITE_O);
       if (__all_sync(0xffffffffu, w)) {
         tc_fence_after();
         const float inv_l = 1.f / l;
@@ -397,7 +457,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ov[32];
-          tmem_ld32(lane_base + O_COL + 32u * c, ov);
+          tmem_ld32(lane_base + o_col + 32u * c, ov);
           tmem_wait_ld();
           reg_fence32(ov);
           uint32_t pk[16];
@@ -408,8 +468,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (store) {
             uint4* dst = reinterpret_cast<uint4*>(args.o + row_off + c * 32);
 #pragma unroll
-            for (int t = 0; t < 4; ++t)
-              dst[t] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
           }
         }
         if (store)
@@ -421,7 +481,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == MMA_WARP) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
