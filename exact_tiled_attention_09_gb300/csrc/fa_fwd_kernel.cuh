@@ -18,8 +18,6 @@
 //               touch lanes 32*(w%4) .. 32*(w%4)+31, so the four warps of a
 //               group cover quarters 2, 3, 0, 1)
 //   warps 6..9  softmax of Q tile 1
-// The MMA warp has the lowest warp index on its scheduler: when its single
-// thread is ready to issue it is not held back behind the softmax warps.
 //
 // MMA order per K/V block j (each S_t buffer holds P_t after the softmax, so
 // S_t of block j+1 is issued only after O_t += P_t V_j of block j):
@@ -148,7 +146,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + C::MISC_OFF);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::MISC_OFF + 4);
 
-  const int warp = threadIdx.x >> 5;
+  const int warp = warp_index_uniform();
   const int lane = threadIdx.x & 31;
   const int L = args.L;
   const int n_ct = args.n_ctiles;
@@ -193,62 +191,78 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, args.status, args.timeout_ns};
 
+  // The producer and MMA warps run their loops with all 32 lanes (uniform
+  // control flow, so loop state stays in uniform registers); every lane
+  // polls the barriers and one elected lane issues the copies, MMAs and
+  // commits (always the same lane, so its commits track its own MMAs).
+  auto warp_wait = [&](uint32_t bar, uint32_t parity, uint32_t site) -> bool {
+    const bool w = mbar_wait(bar, parity, ctl, site);
+    return __all_sync(0xffffffffu, w);
+  };
+
   if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    if (elect_one()) {
       mbar_arrive_expect_tx(bar_q, TILES_PER_CTA * C::TILE_BYTES);
       for (int t = 0; t < TILES_PER_CTA; ++t)
         for (int c = 0; c < C::BOXES; ++c)
           tma_load_3d(sQ + t * C::TILE_BYTES + c * BOX_BYTES, &tmQ, bar_q, c * 64,
                       row_base + t * BLOCK_M, bh);
-      int cnt = 0;
-      bool ok = true;
-      auto load = [&](const CUtensorMap* map, int j) -> bool {
-        const int s = cnt % C::NSLOT;
-        const uint32_t use = static_cast<uint32_t>(cnt / C::NSLOT);
-        if (!mbar_wait(bar_empty(s), (use & 1u) ^ 1u, ctl, SITE_EMPTY)) return false;
+    }
+    __syncwarp();
+    int cnt = 0;
+    bool ok = true;
+    auto load = [&](const CUtensorMap* map, int j) -> bool {
+      const int s = cnt % C::NSLOT;
+      const uint32_t use = static_cast<uint32_t>(cnt / C::NSLOT);
+      if (!warp_wait(bar_empty(s), (use & 1u) ^ 1u, SITE_EMPTY)) return false;
+      if (elect_one()) {
         mbar_arrive_expect_tx(bar_full(s), C::TILE_BYTES);
         const uint32_t dst = ring + s * C::TILE_BYTES;
         for (int c = 0; c < C::BOXES; ++c)
           tma_load_3d(dst + c * BOX_BYTES, map, bar_full(s), c * 64, j * BLOCK_N, bh);
-        ++cnt;
-        return true;
-      };
-      // Ring positions: K_j at 2j, V_j at 2j + 1 (the MMA warp's first uses
-      // come in this order).
-      for (int j = 0; j < n_blk && ok; ++j) {
-        ok = load(&tmK, j);
-        if (ok) ok = load(&tmV, j);
       }
-      if (!ok) {
-        // Let every copy already issued land before the CTA exits.
-        mbar_wait_drain(bar_q, 0, args.timeout_ns);
-        for (int s = 0; s < C::NSLOT; ++s) {
-          const int issued = cnt > s ? (cnt - 1 - s) / C::NSLOT + 1 : 0;
-          if (issued > 0) mbar_wait_drain(bar_full(s), (issued - 1) & 1, args.timeout_ns);
-        }
+      __syncwarp();
+      ++cnt;
+      return true;
+    };
+    // Ring positions: K_j at 2j, V_j at 2j + 1 (the MMA warp's first uses
+    // come in this order).
+    for (int j = 0; j < n_blk && ok; ++j) {
+      ok = load(&tmK, j);
+      if (ok) ok = load(&tmV, j);
+    }
+    if (!ok && lane == 0) {
+      // Let every copy already issued land before the CTA exits.
+      mbar_wait_drain(bar_q, 0, args.timeout_ns);
+      for (int s = 0; s < C::NSLOT; ++s) {
+        const int issued = cnt > s ? (cnt - 1 - s) / C::NSLOT + 1 : 0;
+        if (issued > 0) mbar_wait_drain(bar_full(s), (issued - 1) & 1, args.timeout_ns);
       }
     }
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t IDESC_S = idesc_bf16_f32(BLOCK_M, BLOCK_N, false);
-      constexpr uint32_t IDESC_O = idesc_bf16_f32(BLOCK_M, D, true);
-      auto n_t = [&](int t) { return t == 0 ? n_blk0 : n_blk1; };
-      bool ok = mbar_wait(bar_q, 0, ctl, SITE_Q);
+    constexpr uint32_t IDESC_S = idesc_bf16_f32(BLOCK_M, BLOCK_N, false);
+    constexpr uint32_t IDESC_O = idesc_bf16_f32(BLOCK_M, D, true);
+    auto n_t = [&](int t) { return t == 0 ? n_blk0 : n_blk1; };
+    bool ok = warp_wait(bar_q, 0, SITE_Q);
+    tc_fence_after();
+    // Wait for ring position `pos` to be filled; returns its slot address.
+    auto acquire = [&](int pos, uint32_t& addr) -> bool {
+      const int s = pos % C::NSLOT;
+      const uint32_t use = static_cast<uint32_t>(pos / C::NSLOT);
+      if (!warp_wait(bar_full(s), use & 1u, SITE_FULL)) return false;
       tc_fence_after();
-      // Wait for ring position `pos` to be filled; returns its slot address.
-      auto acquire = [&](int pos, uint32_t& addr) -> bool {
-        const int s = pos % C::NSLOT;
-        const uint32_t use = static_cast<uint32_t>(pos / C::NSLOT);
-        if (!mbar_wait(bar_full(s), use & 1u, ctl, SITE_FULL)) return false;
-        tc_fence_after();
-        addr = ring + s * C::TILE_BYTES;
-        return true;
-      };
-      auto release = [&](int pos) { mma_commit(bar_empty(pos % C::NSLOT)); };
-      auto issue_s = [&](int t, uint32_t kaddr) {
-        const uint32_t q = sQ + t * C::TILE_BYTES;
+      addr = ring + s * C::TILE_BYTES;
+      return true;
+    };
+    auto release = [&](int pos) {
+      if (elect_one()) mma_commit(bar_empty(pos % C::NSLOT));
+      __syncwarp();
+    };
+    auto issue_s = [&](int t, uint32_t kaddr) {
+      const uint32_t q = sQ + t * C::TILE_BYTES;
+      if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
@@ -256,10 +270,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                  sdesc_sw128(kaddr + off, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar_s(t));
-      };
-      auto issue_pv = [&](int t, int j, uint32_t vaddr) -> bool {
-        if (!mbar_wait(bar_p(t), j & 1, ctl, SITE_P)) return false;
-        tc_fence_after();
+      }
+      __syncwarp();
+    };
+    auto issue_pv = [&](int t, int j, uint32_t vaddr) -> bool {
+      if (!warp_wait(bar_p(t), j & 1, SITE_P)) return false;
+      tc_fence_after();
+      if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < BLOCK_N / 16; ++kk) {
           mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + kk * 8,
@@ -267,41 +284,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                  (j > 0 || kk > 0) ? 1u : 0u);
         }
         if (j == n_t(t) - 1) mma_commit(bar_o(t));
-        return true;
-      };
+      }
+      __syncwarp();
+      return true;
+    };
 
-      uint32_t kaddr = 0, vaddr = 0;
-      if (ok && n_blk > 0) {
-        ok = acquire(0, kaddr);
-        if (ok) {
-          for (int t = 0; t < TILES_PER_CTA; ++t)
-            if (n_t(t) > 0) issue_s(t, kaddr);
-          release(0);
+    uint32_t kaddr = 0, vaddr = 0;
+    if (ok && n_blk > 0) {
+      ok = acquire(0, kaddr);
+      if (ok) {
+        for (int t = 0; t < TILES_PER_CTA; ++t)
+          if (n_t(t) > 0) issue_s(t, kaddr);
+        release(0);
+      }
+    }
+    for (int j = 0; j < n_blk && ok; ++j) {
+      ok = acquire(2 * j + 1, vaddr);
+      // K_{j+1} is taken just before its first use, so PV0_j never waits
+      // for it.  Some tile uses K_{j+1} whenever j + 1 < n_blk.
+      bool k_next = false;
+      for (int t = 0; t < TILES_PER_CTA && ok; ++t) {
+        if (j < n_t(t)) ok = issue_pv(t, j, vaddr);
+        if (ok && j + 1 < n_t(t)) {
+          if (!k_next) ok = acquire(2 * j + 2, kaddr);
+          k_next = true;
+          if (ok) issue_s(t, kaddr);
         }
       }
-      for (int j = 0; j < n_blk && ok; ++j) {
-        ok = acquire(2 * j + 1, vaddr);
-        // K_{j+1} is taken just before its first use, so PV0_j never waits
-        // for it.  Some tile uses K_{j+1} whenever j + 1 < n_blk.
-        bool k_next = false;
-        for (int t = 0; t < TILES_PER_CTA && ok; ++t) {
-          if (j < n_t(t)) ok = issue_pv(t, j, vaddr);
-          if (ok && j + 1 < n_t(t)) {
-            if (!k_next) ok = acquire(2 * j + 2, kaddr);
-            k_next = true;
-            if (ok) issue_s(t, kaddr);
-          }
-        }
-        if (ok) {
-          release(2 * j + 1);
-          if (k_next) release(2 * j + 2);
-        }
+      if (ok) {
+        release(2 * j + 1);
+        if (k_next) release(2 * j + 2);
       }
-      if (!ok) {
-        // Every MMA already issued must finish before the tensor memory is freed.
+    }
+    if (!ok) {
+      // Every MMA already issued must finish before the tensor memory is freed.
+      if (elect_one()) {
         mma_commit(bar_drain);
         mbar_wait_drain(bar_drain, 0, args.timeout_ns);
       }
+      __syncwarp();
     }
   } else {
     // ------------------------------------------------------------ softmax
