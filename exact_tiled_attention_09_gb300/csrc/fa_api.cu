@@ -124,6 +124,13 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   args.lse = lse;
   args.L = L;
   args.n_ctiles = static_cast<int>(n_ct);
+  args.bh = static_cast<int>(BH);
+  {
+    // Heads per scheduling group: K + V of a group within ~32 MB of L2.
+    const int64_t kv_bytes = static_cast<int64_t>(L) * d * 2 * 2;
+    const int64_t g = kv_bytes > 0 ? (int64_t{32} << 20) / kv_bytes : BH;
+    args.group_heads = static_cast<int>(g < 1 ? 1 : (g > BH ? BH : g));
+  }
   args.scale_log2 = scale * 1.4426950408889634f;
   args.status = status;
   args.timeout_ns = g_timeout_ns;

@@ -11,9 +11,11 @@
 // re-targeted here to tcgen05 and tensor memory).
 //
 // Warp roles (320 threads):
-//   warp 0      MMA issuer (one thread) and owner of the tensor memory
-//   warp 1      TMA producer: loads Q0 and Q1 once, then K_j and V_j tiles
-//               into a ring of shared-memory slots (full/empty mbarriers)
+//   warp 0      MMA issuer and owner of the tensor memory: all 32 lanes run
+//               the loop and poll the barriers, one elected lane issues
+//   warp 1      TMA producer (same scheme): loads Q0 and Q1 once, then K_j
+//               and V_j tiles into a ring of shared-memory slots (full/empty
+//               mbarriers)
 //   warps 2..5  softmax of Q tile 0 (row r = TMEM lane r; warp w may only
 //               touch lanes 32*(w%4) .. 32*(w%4)+31, so the four warps of a
 //               group cover quarters 2, 3, 0, 1)
@@ -98,6 +100,8 @@ struct FwdArgs {
   float* lse;         // fp32 [BH, L]
   int L;
   int n_ctiles;       // ceil(L / ROWS_PER_CTA)
+  int bh;             // B * H
+  int group_heads;    // heads per scheduling group (see the CTA order)
   float scale_log2;   // scale * log2(e)
   unsigned int* status;
   unsigned long long timeout_ns;
@@ -151,11 +155,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int L = args.L;
   const int n_ct = args.n_ctiles;
 
-  // CTA order: head-major, so the CTAs resident at one time share the K/V of
-  // a few heads in L2.  Causal: the heaviest (last) rows of a head first.
-  const int bh = static_cast<int>(blockIdx.x) / n_ct;
-  const int ct_raw = static_cast<int>(blockIdx.x) % n_ct;
-  const int ct = CAUSAL ? (n_ct - 1 - ct_raw) : ct_raw;
+  // CTA order.  Heads are taken in groups of `group_heads` whose K and V
+  // together fit comfortably in L2, so the CTAs resident at one time re-read
+  // K/V from L2, not HBM.  Non-causal CTAs all cost the same and go
+  // head-major.  Causal CTAs cost in proportion to their row index, so
+  // within a group the longest go first across all of the group's heads
+  // (longest-processing-time order), which keeps the tail of the launch
+  // short.
+  const int BH = args.bh;
+  const int G = args.group_heads;
+  const int idx = static_cast<int>(blockIdx.x);
+  const int g0 = (idx / (G * n_ct)) * G;           // first head of the group
+  const int gsz = min(G, BH - g0);                 // heads in this group
+  const int r = idx - g0 * n_ct;                   // rank within the group
+  const int bh = CAUSAL ? g0 + r % gsz : g0 + r / n_ct;
+  const int ct = CAUSAL ? n_ct - 1 - r / gsz : r % n_ct;
   const int row_base = ct * ROWS_PER_CTA;
   const int n_blk0 = blocks_for_tile<CAUSAL>(row_base, L);
   const int n_blk1 = blocks_for_tile<CAUSAL>(row_base + BLOCK_M, L);
