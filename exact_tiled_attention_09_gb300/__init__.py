@@ -22,8 +22,9 @@ from .build import LIB
 __all__ = [
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED_D", "FA_ERR_MISALIGNED",
     "FA_ERR_DEVICE", "FA_ERR_LAUNCH", "FA_ERR_TIMEOUT", "FAError",
-    "library", "fa_fwd", "fa_device_status", "fa_set_wait_timeout_ns", "fa_status_string",
-    "fa_version", "forward", "flops",
+    "library", "fa_fwd", "fa_fwd_splitkv", "fa_splitkv_workspace_bytes", "fa_device_status",
+    "fa_set_wait_timeout_ns", "fa_status_string", "fa_version", "forward", "forward_splitkv",
+    "flops",
 ]
 
 FA_OK = 0
@@ -57,6 +58,11 @@ def library() -> ctypes.CDLL:
         vp, ci = ctypes.c_void_p, ctypes.c_int
         lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ctypes.c_float, ci, vp]
         lib.fa_fwd.restype = ci
+        lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ctypes.c_float, ci, ci,
+                                       vp, ctypes.c_size_t, vp]
+        lib.fa_fwd_splitkv.restype = ci
+        lib.fa_splitkv_workspace_bytes.argtypes = [ci, ci, ci, ci, ci]
+        lib.fa_splitkv_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_device_status.argtypes = [vp, ci]
         lib.fa_device_status.restype = ci
         lib.fa_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
@@ -73,6 +79,17 @@ def library() -> ctypes.CDLL:
 def fa_fwd(q, k, v, o, lse, B, H, L, d, scale, causal, stream) -> int:
     """Direct call of the C entry point with integer device addresses."""
     return library().fa_fwd(q, k, v, o, lse, B, H, L, d, scale, causal, stream)
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, B, H, L, d, scale, causal, n_splits, workspace,
+                   workspace_bytes, stream) -> int:
+    """Direct call of the split-KV C entry point with integer addresses."""
+    return library().fa_fwd_splitkv(q, k, v, o, lse, B, H, L, d, scale, causal, n_splits,
+                                    workspace, workspace_bytes, stream)
+
+
+def fa_splitkv_workspace_bytes(B, H, L, d, n_splits) -> int:
+    return library().fa_splitkv_workspace_bytes(B, H, L, d, n_splits)
 
 
 def fa_device_status(stream=None, clear=True) -> int:
@@ -129,4 +146,43 @@ def forward(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
                     B, H, L, d, float(scale), int(bool(causal)), stream.cuda_stream)
     if rc != FA_OK:
         raise FAError(rc)
+    return out, lse
+
+
+def forward_splitkv(q, k, v, n_splits, scale=None, causal=False, out=None, lse=None,
+                    workspace=None, stream=None):
+    """:func:`forward` computed in ``n_splits`` key splits plus a merge.
+
+    ``workspace`` (a CUDA uint8 tensor of at least
+    ``fa_splitkv_workspace_bytes(B, H, L, d, n_splits)`` bytes, 256-byte
+    aligned) is allocated here when not given.
+    """
+    import torch
+
+    if q.shape != k.shape or q.shape != v.shape or q.dim() != 4:
+        raise ValueError("q, k, v must share one shape [B, H, L, d]")
+    for t in (q, k, v):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous CUDA bfloat16 tensors")
+    B, H, L, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = fa_splitkv_workspace_bytes(B, H, L, d, n_splits)
+    if need == 0:
+        raise ValueError("invalid sizes or n_splits for split-KV")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, L), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        rc = fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                            lse.data_ptr(), B, H, L, d, float(scale), int(bool(causal)),
+                            int(n_splits), workspace.data_ptr(),
+                            workspace.numel() * workspace.element_size(), stream.cuda_stream)
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd_splitkv")
     return out, lse

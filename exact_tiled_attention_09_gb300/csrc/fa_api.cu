@@ -10,6 +10,7 @@
 
 #include "fa.h"
 #include "fa_fwd_kernel.cuh"
+#include "fa_merge.cuh"
 
 namespace fa {
 
@@ -58,38 +59,55 @@ bool encode_map(CUtensorMap* map, const void* ptr, int BH, int L, int D) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool CAUSAL>
+template <typename Kernel>
+bool configure_once(Kernel kernel, int smem, int dev, bool* configured, std::mutex& mu) {
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 0 || dev >= kMaxDevices) return false;
+  if (!configured[dev]) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return false;
+    configured[dev] = true;
+  }
+  return true;
+}
+
+template <int D, bool CAUSAL, bool SPLIT>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-           const FwdArgs& args, int BH, cudaStream_t stream, int dev) {
-  auto kernel = fa_fwd_kernel<D, CAUSAL>;
+           const FwdArgs& args, int n_splits, cudaStream_t stream, int dev) {
+  auto kernel = fa_fwd_kernel<D, CAUSAL, SPLIT>;
   constexpr int smem = FwdCfg<D>::SMEM_BYTES;
   static bool configured[kMaxDevices] = {};
   static std::mutex mu;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_DEVICE;
-    if (!configured[dev]) {
-      if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-          cudaSuccess)
-        return FA_ERR_LAUNCH;
-      configured[dev] = true;
-    }
-  }
-  const dim3 grid(static_cast<unsigned>(args.n_ctiles) * static_cast<unsigned>(BH));
+  if (!configure_once(kernel, smem, dev, configured, mu)) return FA_ERR_LAUNCH;
+  const dim3 grid(static_cast<unsigned>(args.n_ctiles) * static_cast<unsigned>(args.bh) *
+                  static_cast<unsigned>(n_splits));
   kernel<<<grid, NUM_THREADS, smem, stream>>>(mq, mk, mv, args);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+template <int D>
+int launch_merge(const FwdArgs& args, int n_splits, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(args.bh) * args.L;
+  const dim3 grid(static_cast<unsigned>((rows + MERGE_WARPS - 1) / MERGE_WARPS));
+  fa_merge_kernel<D><<<grid, MERGE_WARPS * 32, 0, stream>>>(args.o_part, args.lse_part, args.o,
+                                                            args.lse, rows, n_splits);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-}  // namespace
-}  // namespace fa
+// Validation shared by every entry point, then the tensor maps and kernel
+// arguments.  Returns FA_OK or the status of the first failed check; nothing
+// is launched here.
+struct Prepared {
+  CUtensorMap mq, mk, mv;
+  FwdArgs args;
+  int dev;
+};
 
-extern "C" {
-
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int L,
-           int d, float scale, int causal, fa_stream_t stream) {
-  using namespace fa;
+int prepare(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int L,
+            int d, float scale, int causal, Prepared* out) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || L < 1) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
@@ -109,19 +127,21 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     return FA_ERR_DEVICE;
   if (major != 10 || minor != 3) return FA_ERR_DEVICE;
 
-  CUtensorMap mq, mk, mv;
-  if (!encode_map(&mq, q, static_cast<int>(BH), L, d) ||
-      !encode_map(&mk, k, static_cast<int>(BH), L, d) ||
-      !encode_map(&mv, v, static_cast<int>(BH), L, d))
+  if (!encode_map(&out->mq, q, static_cast<int>(BH), L, d) ||
+      !encode_map(&out->mk, k, static_cast<int>(BH), L, d) ||
+      !encode_map(&out->mv, v, static_cast<int>(BH), L, d))
     return FA_ERR_LAUNCH;
 
   unsigned int* status = nullptr;
   if (cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_status) != cudaSuccess)
     return FA_ERR_LAUNCH;
 
-  FwdArgs args;
+  FwdArgs& args = out->args;
   args.o = static_cast<uint16_t*>(o);
   args.lse = lse;
+  args.blocks_per_split = 0;
+  args.o_part = nullptr;
+  args.lse_part = nullptr;
   args.L = L;
   args.n_ctiles = static_cast<int>(n_ct);
   args.bh = static_cast<int>(BH);
@@ -134,14 +154,89 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   args.scale_log2 = scale * 1.4426950408889634f;
   args.status = status;
   args.timeout_ns = g_timeout_ns;
+  out->dev = dev;
+  return FA_OK;
+}
 
+// Effective split count: no more splits than K/V blocks, and no split left
+// without a block (blocks_per_split = ceil(blocks / splits)).
+void split_plan(int L, int n_splits, int* eff_splits, int* blocks_per_split) {
+  const int blocks = (L + BLOCK_N - 1) / BLOCK_N;
+  int ns = n_splits < blocks ? n_splits : blocks;
+  const int bps = (blocks + ns - 1) / ns;
+  ns = (blocks + bps - 1) / bps;
+  *eff_splits = ns;
+  *blocks_per_split = bps;
+}
+
+constexpr int kMaxSplits = 64;
+
+size_t align256(size_t x) { return (x + 255) & ~size_t{255}; }
+
+size_t workspace_bytes(int64_t BH, int L, int d, int n_splits) {
+  const size_t rows = static_cast<size_t>(BH) * static_cast<size_t>(L);
+  return align256(static_cast<size_t>(n_splits) * rows * d * 4) +
+         static_cast<size_t>(n_splits) * rows * 4;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int L,
+           int d, float scale, int causal, fa_stream_t stream) {
+  using namespace fa;
+  Prepared p;
+  const int rc = prepare(q, k, v, o, lse, B, H, L, d, scale, causal, &p);
+  if (rc != FA_OK) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const int bh = static_cast<int>(BH);
   if (d == 64)
-    return causal ? launch<64, true>(mq, mk, mv, args, bh, s, dev)
-                  : launch<64, false>(mq, mk, mv, args, bh, s, dev);
-  return causal ? launch<128, true>(mq, mk, mv, args, bh, s, dev)
-                : launch<128, false>(mq, mk, mv, args, bh, s, dev);
+    return causal ? launch<64, true, false>(p.mq, p.mk, p.mv, p.args, 1, s, p.dev)
+                  : launch<64, false, false>(p.mq, p.mk, p.mv, p.args, 1, s, p.dev);
+  return causal ? launch<128, true, false>(p.mq, p.mk, p.mv, p.args, 1, s, p.dev)
+                : launch<128, false, false>(p.mq, p.mk, p.mv, p.args, 1, s, p.dev);
+}
+
+size_t fa_splitkv_workspace_bytes(int B, int H, int L, int d, int n_splits) {
+  if (B < 1 || H < 1 || L < 1 || (d != 64 && d != 128) || n_splits < 1 ||
+      n_splits > fa::kMaxSplits)
+    return 0;
+  return fa::workspace_bytes(static_cast<int64_t>(B) * H, L, d, n_splits);
+}
+
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                   int L, int d, float scale, int causal, int n_splits, void* workspace,
+                   size_t workspace_bytes_given, fa_stream_t stream) {
+  using namespace fa;
+  if (n_splits < 1 || n_splits > kMaxSplits || !workspace) return FA_ERR_INVALID_ARG;
+  if (B >= 1 && H >= 1 && L >= 1 && (d == 64 || d == 128)) {
+    if (workspace_bytes_given < workspace_bytes(static_cast<int64_t>(B) * H, L, d, n_splits))
+      return FA_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return FA_ERR_MISALIGNED;
+  }
+  Prepared p;
+  const int rc = prepare(q, k, v, o, lse, B, H, L, d, scale, causal, &p);
+  if (rc != FA_OK) return rc;
+  int ns = 1, bps = 1;
+  split_plan(L, n_splits, &ns, &bps);
+  if (static_cast<int64_t>(p.args.bh) * p.args.n_ctiles * ns > 0x7fffffff)
+    return FA_ERR_INVALID_ARG;
+  const size_t rows = static_cast<size_t>(p.args.bh) * static_cast<size_t>(L);
+  p.args.blocks_per_split = bps;
+  p.args.o_part = static_cast<float*>(workspace);
+  p.args.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                             align256(static_cast<size_t>(ns) * rows * d * 4));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int r;
+  if (d == 64)
+    r = causal ? launch<64, true, true>(p.mq, p.mk, p.mv, p.args, ns, s, p.dev)
+               : launch<64, false, true>(p.mq, p.mk, p.mv, p.args, ns, s, p.dev);
+  else
+    r = causal ? launch<128, true, true>(p.mq, p.mk, p.mv, p.args, ns, s, p.dev)
+               : launch<128, false, true>(p.mq, p.mk, p.mv, p.args, ns, s, p.dev);
+  if (r != FA_OK) return r;
+  return d == 64 ? launch_merge<64>(p.args, ns, s) : launch_merge<128>(p.args, ns, s);
 }
 
 int fa_device_status(fa_stream_t stream, int clear) {

@@ -98,6 +98,11 @@ struct FwdCfg {
 struct FwdArgs {
   uint16_t* o;        // bf16 [BH, L, D]
   float* lse;         // fp32 [BH, L]
+  // Split-KV only: K/V blocks per split, and the per-split results
+  // (normalised over the split's keys) the merge kernel combines.
+  int blocks_per_split;
+  float* o_part;      // fp32 [n_splits, BH, L, D]
+  float* lse_part;    // fp32 [n_splits, BH, L]
   int L;
   int n_ctiles;       // ceil(L / ROWS_PER_CTA)
   int bh;             // B * H
@@ -127,7 +132,11 @@ __device__ __forceinline__ int blocks_for_tile(int row0, int L) {
   return CAUSAL ? min(all, (row0 + BLOCK_M - 1) / BLOCK_N + 1) : all;
 }
 
-template <int D, bool CAUSAL>
+// SPLIT: the CTA covers only K/V blocks [split * blocks_per_split,
+// (split + 1) * blocks_per_split) of its rows and writes fp32 partial results
+// (Flash-Decoding's per-chunk pass, "04 Transformers, Attention, and
+// FlashAttention", Flash-Decoding); the merge kernel finishes them.
+template <int D, bool CAUSAL, bool SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
@@ -164,15 +173,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // short.
   const int BH = args.bh;
   const int G = args.group_heads;
-  const int idx = static_cast<int>(blockIdx.x);
+  const int n_units = BH * n_ct;                   // CTAs per split
+  const int split = SPLIT ? static_cast<int>(blockIdx.x) / n_units : 0;
+  const int idx = static_cast<int>(blockIdx.x) - split * n_units;
   const int g0 = (idx / (G * n_ct)) * G;           // first head of the group
   const int gsz = min(G, BH - g0);                 // heads in this group
   const int r = idx - g0 * n_ct;                   // rank within the group
   const int bh = CAUSAL ? g0 + r % gsz : g0 + r / n_ct;
   const int ct = CAUSAL ? n_ct - 1 - r / gsz : r % n_ct;
   const int row_base = ct * ROWS_PER_CTA;
-  const int n_blk0 = blocks_for_tile<CAUSAL>(row_base, L);
-  const int n_blk1 = blocks_for_tile<CAUSAL>(row_base + BLOCK_M, L);
+  // Block range of this CTA: [jb, jb + n_blk); every loop below counts
+  // blocks from jb (barrier phases and ring positions use the local count).
+  int nb0 = blocks_for_tile<CAUSAL>(row_base, L);
+  int nb1 = blocks_for_tile<CAUSAL>(row_base + BLOCK_M, L);
+  int jb = 0;
+  if (SPLIT) {
+    jb = split * args.blocks_per_split;
+    const int je = jb + args.blocks_per_split;
+    nb0 = max(0, min(nb0, je) - jb);
+    nb1 = max(0, min(nb1, je) - jb);
+  }
+  const int n_blk0 = nb0;
+  const int n_blk1 = nb1;
   const int n_blk = max(n_blk0, n_blk1);  // K/V blocks loaded
 
   if (threadIdx.x == 0) {
@@ -234,7 +256,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_arrive_expect_tx(bar_full(s), C::TILE_BYTES);
         const uint32_t dst = ring + s * C::TILE_BYTES;
         for (int c = 0; c < C::BOXES; ++c)
-          tma_load_3d(dst + c * BOX_BYTES, map, bar_full(s), c * 64, j * BLOCK_N, bh);
+          tma_load_3d(dst + c * BOX_BYTES, map, bar_full(s), c * 64, (jb + j) * BLOCK_N, bh);
       }
       __syncwarp();
       ++cnt;
@@ -370,7 +392,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int c = 0; c < 4; ++c) reg_fence32(sr[c]);
 
       // Masks: keys past the end of the sequence; causal keys after the query.
-      const int k0 = j * BLOCK_N;
+      const int k0 = (jb + j) * BLOCK_N;
       const bool need_mask = (k0 + BLOCK_N > L) || (CAUSAL && k0 + BLOCK_N - 1 > tile_row0);
       if (need_mask) {
 #pragma unroll
@@ -481,35 +503,63 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) mbar_arrive(bar_p(t));
     }
 
+    const bool store = q_row < L;
     if (ok && n_my > 0) {
       // Epilogue: wait for the last O_t += P_t V, then O / l and LSE.
       const bool w = mbar_wait(bar_o(t), 0, ctl, SITE_O);
       if (__all_sync(0xffffffffu, w)) {
         tc_fence_after();
         const float inv_l = 1.f / l;
-        const bool store = q_row < L;
-        const size_t row_off = (static_cast<size_t>(bh) * L + q_row) * D;
+        const float lse_row = (m + log2f(l)) * 0.69314718055994531f;
+        const size_t row = static_cast<size_t>(bh) * L + q_row;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ov[32];
           tmem_ld32(lane_base + o_col + 32u * c, ov);
           tmem_wait_ld();
           reg_fence32(ov);
-          uint32_t pk[16];
+          if constexpr (SPLIT) {
+            // fp32 partial, normalised over this split's keys.
+            if (store) {
+              float4* dst = reinterpret_cast<float4*>(
+                  args.o_part + (static_cast<size_t>(split) * args.bh * L + row) * D + c * 32);
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv_l,
-                                __uint_as_float(ov[2 * e + 1]) * inv_l);
-          if (store) {
-            uint4* dst = reinterpret_cast<uint4*>(args.o + row_off + c * 32);
+              for (int i = 0; i < 8; ++i)
+                dst[i] = make_float4(__uint_as_float(ov[4 * i]) * inv_l,
+                                     __uint_as_float(ov[4 * i + 1]) * inv_l,
+                                     __uint_as_float(ov[4 * i + 2]) * inv_l,
+                                     __uint_as_float(ov[4 * i + 3]) * inv_l);
+            }
+          } else {
+            uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            for (int e = 0; e < 16; ++e)
+              pk[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv_l,
+                                  __uint_as_float(ov[2 * e + 1]) * inv_l);
+            if (store) {
+              uint4* dst = reinterpret_cast<uint4*>(args.o + row * D + c * 32);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
           }
         }
-        if (store)
-          args.lse[static_cast<size_t>(bh) * L + q_row] = (m + log2f(l)) * 0.69314718055994531f;
+        if (store) {
+          if constexpr (SPLIT)
+            args.lse_part[static_cast<size_t>(split) * args.bh * L + row] = lse_row;
+          else
+            args.lse[row] = lse_row;
+        }
       }
+    } else if (SPLIT && ok && store) {
+      // No key of this split is visible to this tile (causal): an empty
+      // partial, weight exp(-inf) = 0 in the merge.
+      const size_t row = static_cast<size_t>(bh) * L + q_row;
+      float4* dst = reinterpret_cast<float4*>(
+          args.o_part + (static_cast<size_t>(split) * args.bh * L + row) * D);
+#pragma unroll
+      for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      args.lse_part[static_cast<size_t>(split) * args.bh * L + row] = -INFINITY;
     }
     tmem_wait_st();
   }

@@ -23,6 +23,7 @@
 #ifndef FA_GB300_FA_H
 #define FA_GB300_FA_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -76,6 +77,43 @@ enum fa_status {
  */
 int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
            int L, int d, float scale, int causal, fa_stream_t stream);
+
+/*
+ * fa_fwd_splitkv -- the same result as fa_fwd, computed in key splits and
+ * merged (Flash-Decoding: "04 Transformers, Attention, and FlashAttention",
+ * section on Flash-Decoding -- split K/V into chunks, attend to each chunk
+ * in parallel, combine the chunk results).  Worth it when B * H * ceil(L/256)
+ * is small next to the number of SMs (few heads, long sequences).
+ *
+ *   q..causal : as for fa_fwd.
+ *   n_splits  : requested number of key splits, 1..64.  The kernel uses
+ *               min(n_splits, ceil(L/128)) splits of whole 128-key blocks.
+ *   workspace : device scratch owned by the caller, 256-byte aligned, at
+ *               least fa_splitkv_workspace_bytes(B, H, L, d, n_splits)
+ *               bytes.  It receives the per-split fp32 partial O and LSE;
+ *               its contents on entry do not matter and are undefined after.
+ *   workspace_bytes : size of that buffer.
+ *
+ * Split s of row i holds O_s, normalised over the split's keys, and LSE_s;
+ * the merge writes LSE = log sum_s exp(LSE_s) and O = sum_s exp(LSE_s - LSE)
+ * O_s (bf16, round to nearest even).  Two kernels are launched on `stream`:
+ * the split pass and the merge; calls that share a workspace on concurrent
+ * streams race.  Errors: those of fa_fwd, plus FA_ERR_INVALID_ARG for
+ * n_splits outside 1..64, a null workspace or one smaller than required,
+ * and FA_ERR_MISALIGNED for a workspace not 256-byte aligned.
+ */
+int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                   int H, int L, int d, float scale, int causal, int n_splits, void *workspace,
+                   size_t workspace_bytes, fa_stream_t stream);
+
+/*
+ * fa_splitkv_workspace_bytes -- bytes of workspace fa_fwd_splitkv needs for
+ * these sizes: 256-byte-aligned room for fp32 partial O [n_splits, B, H, L, d]
+ * followed by fp32 partial LSE [n_splits, B, H, L].  Returns 0 for invalid
+ * sizes (B/H/L < 1, d not 64/128, n_splits outside 1..64).  Host only; no
+ * CUDA call.
+ */
+size_t fa_splitkv_workspace_bytes(int B, int H, int L, int d, int n_splits);
 
 /*
  * fa_device_status -- synchronise `stream` and report whether any kernel of

@@ -113,3 +113,37 @@ def test_product_path_does_not_import_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 src = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in src, f
+
+
+def test_splitkv_workspace_bytes(lib):
+    B, H, L, d, S = 2, 3, 300, 64, 5
+    rows = B * H * L
+    o_bytes = S * rows * d * 4
+    expect = ((o_bytes + 255) // 256) * 256 + S * rows * 4
+    assert fa.fa_splitkv_workspace_bytes(B, H, L, d, S) == expect
+    assert fa.fa_splitkv_workspace_bytes(B, H, L, 96, S) == 0
+    assert fa.fa_splitkv_workspace_bytes(B, H, L, d, 0) == 0
+    assert fa.fa_splitkv_workspace_bytes(B, H, L, d, 65) == 0
+    assert fa.fa_splitkv_workspace_bytes(0, H, L, d, S) == 0
+
+
+def _call_split(ws=0x1000000, ws_bytes=None, n_splits=4, **over):
+    a = dict(GOOD)
+    a.update(over)
+    if ws_bytes is None:
+        ws_bytes = fa.fa_splitkv_workspace_bytes(a["B"], a["H"], a["L"], a["d"], max(1, n_splits))
+    return fa.fa_fwd_splitkv(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["L"],
+                             a["d"], a["scale"], a["causal"], n_splits, ws, ws_bytes, None)
+
+
+def test_splitkv_validation_launches_nothing(lib):
+    assert _call_split(n_splits=0, ws_bytes=1 << 30) == fa.FA_ERR_INVALID_ARG
+    assert _call_split(n_splits=65, ws_bytes=1 << 30) == fa.FA_ERR_INVALID_ARG
+    assert _call_split(ws=0) == fa.FA_ERR_INVALID_ARG
+    assert _call_split(ws_bytes=100) == fa.FA_ERR_INVALID_ARG
+    assert _call_split(ws=0x1000010) == fa.FA_ERR_MISALIGNED
+    assert _call_split(q=0) == fa.FA_ERR_INVALID_ARG
+    assert _call_split(d=96) == fa.FA_ERR_UNSUPPORTED_D
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        assert _call_split() == fa.FA_ERR_DEVICE

@@ -324,3 +324,29 @@ def test_oracle_rejects_bad_arguments():
         oracle.attention(q, q, q, 1.0, rows=[4 * 1 + 7])
     with pytest.raises(ValueError):
         oracle.attention(q, q[:3], q, 1.0)
+
+
+# --------------------------------------------------------------------------
+# P8. Flash-Decoding ("04 Transformers, Attention, and FlashAttention",
+#     Flash-Decoding): attention over key chunks, merged by their log-sum-exp
+#     weights, equals attention over all keys.  Pins the merge rule the
+#     split-KV path uses, with the oracle on each chunk.
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("cuts", [(25,), (1, 49), (10, 20, 30, 40), (49,)])
+def test_split_and_merge_equals_whole(cuts):
+    L, d = 50, 8
+    q, k, v = _bf16_normals((L, d), 21, std=2.0)
+    o_all, lse_all = oracle.attention(q, k, v, 0.5)
+    bounds = [0, *cuts, L]
+    # each chunk: every query against keys [lo, hi) only (non-causal, so the
+    # oracle's matrix statement takes a key block of its own length)
+    parts = [oracle.attention_numpy(q, k[lo:hi], v[lo:hi], 0.5)
+             for lo, hi in zip(bounds[:-1], bounds[1:])]
+    lses = np.stack([p[1] for p in parts])
+    M = lses.max(axis=0)
+    lse = M + np.log(np.exp(lses - M).sum(axis=0))
+    o = sum(np.exp(p[1] - lse)[:, None] * p[0] for p in parts)
+    assert np.abs(lse - lse_all).max() <= 1e-12
+    assert np.abs(o - o_all).max() <= 1e-12
+    # an empty chunk (log-sum-exp -inf) has weight exp(-inf - lse) = 0
+    assert np.exp(-np.inf - lse).max() == 0.0
