@@ -22,7 +22,8 @@ from .build import LIB
 __all__ = [
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED_D", "FA_ERR_MISALIGNED",
     "FA_ERR_DEVICE", "FA_ERR_LAUNCH", "FA_ERR_TIMEOUT", "FAError",
-    "library", "fa_fwd", "fa_fwd_splitkv", "fa_splitkv_workspace_bytes", "fa_device_status",
+    "library", "fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_static", "FA_STATIC_WORKSPACE_BYTES",
+    "fa_splitkv_workspace_bytes", "fa_device_status",
     "fa_set_wait_timeout_ns", "fa_status_string", "fa_version", "forward", "forward_splitkv",
     "flops",
 ]
@@ -61,6 +62,9 @@ def library() -> ctypes.CDLL:
         lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ctypes.c_float, ci, ci,
                                        vp, ctypes.c_size_t, vp]
         lib.fa_fwd_splitkv.restype = ci
+        lib.fa_fwd_splitkv_static.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ctypes.c_float,
+                                              ci, ci, vp]
+        lib.fa_fwd_splitkv_static.restype = ci
         lib.fa_splitkv_workspace_bytes.argtypes = [ci, ci, ci, ci, ci]
         lib.fa_splitkv_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_device_status.argtypes = [vp, ci]
@@ -86,6 +90,17 @@ def fa_fwd_splitkv(q, k, v, o, lse, B, H, L, d, scale, causal, n_splits, workspa
     """Direct call of the split-KV C entry point with integer addresses."""
     return library().fa_fwd_splitkv(q, k, v, o, lse, B, H, L, d, scale, causal, n_splits,
                                     workspace, workspace_bytes, stream)
+
+
+def fa_fwd_splitkv_static(q, k, v, o, lse, B, H, L, d, scale, causal, n_splits, stream) -> int:
+    """Split-KV on the library's own static scratch array (no workspace, no
+    allocation); for callers that cannot allocate device memory."""
+    return library().fa_fwd_splitkv_static(q, k, v, o, lse, B, H, L, d, scale, causal,
+                                           n_splits, stream)
+
+
+# Size of the static scratch array behind fa_fwd_splitkv_static (fa.h).
+FA_STATIC_WORKSPACE_BYTES = 64 << 20
 
 
 def fa_splitkv_workspace_bytes(B, H, L, d, n_splits) -> int:

@@ -182,6 +182,42 @@ size_t workspace_bytes(int64_t BH, int L, int d, int n_splits) {
 }  // namespace
 }  // namespace fa
 
+// ------------------------------------------------------------------------
+// Split-KV without caller-provided scratch.
+//
+// Some callers cannot allocate device memory at the point where they run
+// attention: a serving engine or plugin host that owns the whole device
+// memory budget and hands out no workspace, or code whose allocator must not
+// be bypassed.  For them the library carries its own split-KV scratch: a
+// fixed FA_STATIC_WORKSPACE_BYTES array in device global memory, created
+// with the module on every GPU that loads this library and kept until the
+// process exits.  The entry point below calls no allocation routine.  On the
+// first call on a device it looks up that device's address of the array
+// (cudaGetSymbolAddress, with the device current) and remembers it; make
+// that first call before any stream capture.  All calls share the one array
+// and it keeps whatever the previous call left there: nothing in it has to
+// start at zero (the split pass writes every partial the merge reads), but
+// calls that overlap on the GPU -- on different streams, or from different
+// host threads -- race on it.
+static __device__ __align__(256) unsigned char g_splitkv_static_ws[FA_STATIC_WORKSPACE_BYTES];
+
+namespace {
+
+void* static_workspace_address(int dev) {
+  static void* addr[fa::kMaxDevices] = {};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 0 || dev >= fa::kMaxDevices) return nullptr;
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_splitkv_static_ws) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
 extern "C" {
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int L,
@@ -237,6 +273,22 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
                : launch<128, false, true>(p.mq, p.mk, p.mv, p.args, ns, s, p.dev);
   if (r != FA_OK) return r;
   return d == 64 ? launch_merge<64>(p.args, ns, s) : launch_merge<128>(p.args, ns, s);
+}
+
+int fa_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o, float* lse,
+                          int B, int H, int L, int d, float scale, int causal, int n_splits,
+                          fa_stream_t stream) {
+  using namespace fa;
+  if (n_splits < 1 || n_splits > kMaxSplits) return FA_ERR_INVALID_ARG;
+  if (B >= 1 && H >= 1 && L >= 1 && (d == 64 || d == 128) &&
+      workspace_bytes(static_cast<int64_t>(B) * H, L, d, n_splits) > FA_STATIC_WORKSPACE_BYTES)
+    return FA_ERR_INVALID_ARG;  // the sizes need more scratch than the static array holds
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_DEVICE;
+  void* ws = static_workspace_address(dev);
+  if (!ws) return FA_ERR_LAUNCH;
+  return fa_fwd_splitkv(q, k, v, o, lse, B, H, L, d, scale, causal, n_splits, ws,
+                        FA_STATIC_WORKSPACE_BYTES, stream);
 }
 
 int fa_device_status(fa_stream_t stream, int clear) {

@@ -116,6 +116,36 @@ int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *
 size_t fa_splitkv_workspace_bytes(int B, int H, int L, int d, int n_splits);
 
 /*
+ * FA_STATIC_WORKSPACE_BYTES -- size of the split-KV scratch array the library
+ * keeps in device memory for fa_fwd_splitkv_static (64 MiB, held on every
+ * GPU that loads the library until the process exits).
+ */
+#define FA_STATIC_WORKSPACE_BYTES ((size_t)64 << 20)
+
+/*
+ * fa_fwd_splitkv_static -- fa_fwd_splitkv for callers that cannot allocate
+ * device memory (an engine or plugin host that owns the whole memory budget
+ * and gives out no scratch): it takes no workspace and calls no allocation
+ * routine; its scratch is the library's own FA_STATIC_WORKSPACE_BYTES array.
+ * The paper has no counterpart to this entry point: it exists only for
+ * callers that cannot hand the library scratch memory.
+ *
+ *   q..n_splits, stream : as for fa_fwd_splitkv.
+ *
+ * Returns FA_ERR_INVALID_ARG, launching nothing, when
+ * fa_splitkv_workspace_bytes(B, H, L, d, n_splits) exceeds
+ * FA_STATIC_WORKSPACE_BYTES (fewer splits, or fa_fwd, then apply), and
+ * otherwise the statuses of fa_fwd_splitkv.  The first call on a device looks
+ * up the array's address on that device (with it current); make that first
+ * call before any stream capture.  Every call uses the same array and finds
+ * it as the previous call left it (nothing in it needs to start at zero), so
+ * calls that overlap on the GPU race.
+ */
+int fa_fwd_splitkv_static(const void *q, const void *k, const void *v, void *o, float *lse,
+                          int B, int H, int L, int d, float scale, int causal, int n_splits,
+                          fa_stream_t stream);
+
+/*
  * fa_device_status -- synchronise `stream` and report whether any kernel of
  * this library on the current device gave up a bounded wait since the status
  * was last cleared (FA_ERR_TIMEOUT) or FA_OK.  A nonzero `clear` resets the
