@@ -18,7 +18,9 @@ LSE back, all inside the timed events.
 ``cpu_baseline`` times the fp64 oracle on the host cores on the same inputs.
 ``workloads`` lists the other synthetic configurations (device-generated
 seeded inputs), each timed the same way, including the d=128 non-causal
-L=8192 point used for the tensor-core fraction.
+L=8192 point used for the tensor-core fraction.  ``splitkv`` times the
+split-KV path (split pass + merge) against the single pass on shapes whose
+single-pass grid underfills the GPU.
 
 With more than one GPU (torchrun) every rank runs its own replica of the
 workload (the forward pass has no exchange step); only the timing is
@@ -212,6 +214,50 @@ def time_forward(fa, torch, q, k, v, w, steps, warmup, flush_buf, o=None, lse=No
     return [s.elapsed_time(e) for s, e in ev]
 
 
+def time_splitkv(fa, torch, q, k, v, w, n_splits, steps, warmup, flush_buf):
+    """Per-step device time (ms) of ``fa.forward_splitkv`` (split pass + merge)."""
+    stream = torch.cuda.current_stream()
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.L), dtype=torch.float32, device=q.device)
+    ws = torch.empty(fa.fa_splitkv_workspace_bytes(w.B, w.H, w.L, w.d, n_splits),
+                     dtype=torch.uint8, device=q.device)
+    run = lambda: fa.forward_splitkv(q, k, v, n_splits, scale=w.scale, causal=w.causal, out=o,
+                                     lse=lse, workspace=ws, stream=stream)
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for s_, e_ in ev:
+        flush_buf.fill_(1)
+        s_.record(stream)
+        run()
+        e_.record(stream)
+    torch.cuda.synchronize()
+    return [s_.elapsed_time(e_) for s_, e_ in ev]
+
+
+def splits_for(w, sms):
+    """Smallest split count that fills one wave of CTAs (two when causal,
+    whose CTAs differ in cost); at most one split per 128-key block and 64."""
+    ctas = w.B * w.H * ((w.L + 255) // 256)
+    blocks = (w.L + 127) // 128
+    target = (2 if w.causal else 1) * sms
+    s = 1
+    while ctas * s < target and s < min(64, blocks):
+        s += 1
+    return s
+
+
+# Shapes whose single-pass grid underfills the GPU (one head, long rows):
+# where the split-KV path is meant to help.
+SPLITKV_SHAPES = [
+    ("B1_H1_L8192_d128", 1, 1, 8192, 128, False),
+    ("B1_H1_L16384_d64", 1, 1, 16384, 64, False),
+    ("B1_H1_L32768_d128_causal", 1, 1, 32768, 128, True),
+]
+
+
 def time_e2e(fa, torch, host, w, steps, warmup, flush_buf, dev):
     """Per-step time (ms) of H2D(Q,K,V) + forward + D2H(O, LSE) from pinned memory."""
     qh, kh, vh = host
@@ -281,6 +327,7 @@ def run_ours(args):
         cpu = cpu_baseline(w, qb, kb, vb)
 
     extras = []
+    splitkv = []
     with ClockSampler(local) as clk:
         if world > 1:
             dist.barrier()
@@ -304,6 +351,23 @@ def run_ours(args):
                                "ms_min": round(min(t), 4), "tflops": round(tf, 1),
                                "frac_of_peak": round(tf / peaks["bf16_tflops"], 4),
                                "steps": steps})
+                del qx, kx, vx
+            from fa_inputs import AttentionWorkload
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            for name, B, H, L, d, causal in SPLITKV_SHAPES:
+                wx = AttentionWorkload(name, B, H, L, d, causal, 1.0 / math.sqrt(d), 100 + L)
+                qx, kx, vx = device_inputs(wx, dev, torch)
+                S = splits_for(wx, sms)
+                steps = max(3, min(args.extra_steps, int(2e13 / wx.flops)))
+                t1 = time_forward(fa, torch, qx, kx, vx, wx, steps, 3, flush_buf)
+                t2 = time_splitkv(fa, torch, qx, kx, vx, wx, S, steps, 3, flush_buf)
+                m1, m2 = sum(t1) / len(t1), sum(t2) / len(t2)
+                splitkv.append({"workload": name, "B": B, "H": H, "L": L, "d": d,
+                                "causal": causal, "n_splits": S,
+                                "single_pass_ms": round(m1, 4), "splitkv_ms": round(m2, 4),
+                                "single_pass_tflops": round(wx.flops / (m1 * 1e-3) / 1e12, 1),
+                                "splitkv_tflops": round(wx.flops / (m2 * 1e-3) / 1e12, 1),
+                                "steps": steps})
                 del qx, kx, vx
     if fa.fa_device_status(None, clear=True) != fa.FA_OK:
         raise RuntimeError("a kernel wait timed out during the benchmark")
@@ -355,6 +419,7 @@ def run_ours(args):
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
             "workloads": extras,
+            "splitkv": splitkv,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
