@@ -24,7 +24,8 @@ __all__ = [
     "FA_ERR_DEVICE", "FA_ERR_LAUNCH", "FA_ERR_TIMEOUT", "FAError",
     "library", "fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_static", "FA_STATIC_WORKSPACE_BYTES",
     "fa_splitkv_workspace_bytes", "fa_device_status",
-    "fa_set_wait_timeout_ns", "fa_status_string", "fa_version", "forward", "forward_splitkv",
+    "fa_set_wait_timeout_ns", "fa_test_withhold_q_load", "fa_status_string", "fa_version",
+    "forward", "forward_splitkv",
     "flops",
 ]
 
@@ -71,6 +72,8 @@ def library() -> ctypes.CDLL:
         lib.fa_device_status.restype = ci
         lib.fa_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
         lib.fa_set_wait_timeout_ns.restype = None
+        lib.fa_test_withhold_q_load.argtypes = [ci]
+        lib.fa_test_withhold_q_load.restype = None
         lib.fa_status_string.argtypes = [ci]
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_version.argtypes = []
@@ -113,6 +116,11 @@ def fa_device_status(stream=None, clear=True) -> int:
 
 def fa_set_wait_timeout_ns(ns: int) -> None:
     library().fa_set_wait_timeout_ns(int(ns))
+
+
+def fa_test_withhold_q_load(enable: bool) -> None:
+    """Test hook of the timeout path (see fa.h); leave disabled otherwise."""
+    library().fa_test_withhold_q_load(int(bool(enable)))
 
 
 def fa_status_string(code: int) -> str:

@@ -20,6 +20,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 unsigned long long g_timeout_ns = 1000000000ull;
+int g_test_withhold_q = 0;
 
 // cuTensorMapEncodeTiled, fetched from the driver through the runtime so the
 // library does not link libcuda directly.
@@ -154,6 +155,7 @@ int prepare(const void* q, const void* k, const void* v, void* o, float* lse, in
   args.scale_log2 = scale * 1.4426950408889634f;
   args.status = status;
   args.timeout_ns = g_timeout_ns;
+  args.test_withhold_q = g_test_withhold_q;
   out->dev = dev;
   return FA_OK;
 }
@@ -305,6 +307,8 @@ int fa_device_status(fa_stream_t stream, int clear) {
 }
 
 void fa_set_wait_timeout_ns(uint64_t ns) { fa::g_timeout_ns = ns < 1000 ? 1000 : ns; }
+
+void fa_test_withhold_q_load(int enable) { fa::g_test_withhold_q = enable ? 1 : 0; }
 
 const char* fa_status_string(int status) {
   switch (status) {

@@ -110,6 +110,7 @@ struct FwdArgs {
   float scale_log2;   // scale * log2(e)
   unsigned int* status;
   unsigned long long timeout_ns;
+  int test_withhold_q;  // test hook: skip the Q copy so the first MMA wait runs out
 };
 
 // Wait that ignores the CTA abort flag (used while draining after an abort).
@@ -238,7 +239,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------ producer
-    if (elect_one()) {
+    if (!args.test_withhold_q && elect_one()) {
       mbar_arrive_expect_tx(bar_q, TILES_PER_CTA * C::TILE_BYTES);
       for (int t = 0; t < TILES_PER_CTA; ++t)
         for (int c = 0; c < C::BOXES; ++c)
@@ -270,7 +271,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     if (!ok && lane == 0) {
       // Let every copy already issued land before the CTA exits.
-      mbar_wait_drain(bar_q, 0, args.timeout_ns);
+      if (!args.test_withhold_q) mbar_wait_drain(bar_q, 0, args.timeout_ns);
       for (int s = 0; s < C::NSLOT; ++s) {
         const int issued = cnt > s ? (cnt - 1 - s) / C::NSLOT + 1 : 0;
         if (issued > 0) mbar_wait_drain(bar_full(s), (issued - 1) & 1, args.timeout_ns);

@@ -162,6 +162,16 @@ int fa_device_status(fa_stream_t stream, int clear);
  */
 void fa_set_wait_timeout_ns(uint64_t ns);
 
+/*
+ * fa_test_withhold_q_load -- test hook for the timeout path.  While enabled
+ * (nonzero), the attention kernels launched afterwards skip their Q copy, so
+ * the MMA warp's first wait never completes: it gives up after the wait
+ * limit, every role stops and drains, the tensor memory is freed and
+ * fa_device_status reports FA_ERR_TIMEOUT.  Outputs of such launches are
+ * undefined.  Process-wide; leave at 0 outside such tests.
+ */
+void fa_test_withhold_q_load(int enable);
+
 /* Human-readable text for a status code (static storage, never NULL). */
 const char *fa_status_string(int status);
 
