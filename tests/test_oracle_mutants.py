@@ -75,3 +75,47 @@ def test_unmodified_definition_passes_the_pins():
                                       "lse_without_max"])
 def test_mutant_is_rejected(mutation):
     assert not _pins_pass(lambda q, k, v, s, c: _definition(q, k, v, s, c, mutation))
+
+
+# --------------------------------------------------------------------------
+# Gradient oracle: each mutant of the backward formulas must fail the pins
+# of tests/test_oracle_bwd_pins.py (finite differences and invariants).
+# --------------------------------------------------------------------------
+def _bwd_definition(q, k, v, dout, scale, causal, mutation=None):
+    L = q.shape[-2]
+    s = scale * (q @ np.swapaxes(k, -1, -2))
+    allowed = np.tril(np.ones((L, L), dtype=bool)) if causal else np.ones((L, L), bool)
+    if mutation != "mask_ignored":
+        s = np.where(allowed, s, -np.inf)
+    e = np.exp(s - s.max(axis=-1, keepdims=True))
+    p = e / e.sum(axis=-1, keepdims=True)
+    pt = np.swapaxes(p, -1, -2)
+    dv = pt @ dout if mutation != "dv_untransposed" else p @ dout
+    dp = dout @ np.swapaxes(v, -1, -2)
+    rowsum = (dp * p).sum(axis=-1, keepdims=True)
+    if mutation == "rowsum_over_keys_axis":
+        rowsum = (dp * p).sum(axis=-2, keepdims=True)
+    ds = p * (dp - rowsum) if mutation != "dropped_rowsum" else p * dp
+    if mutation == "sign_flip":
+        ds = p * (rowsum - dp)
+    dst = np.swapaxes(ds, -1, -2)
+    dq = scale * (ds @ k) if mutation != "dq_transposed" else scale * (dst @ k)
+    dk = scale * (dst @ q)
+    if mutation == "dk_unscaled":
+        dk = dst @ q
+    if mutation == "dk_uses_k":
+        dk = scale * (dst @ k)
+    return dq, dk, dv
+
+
+def test_unmodified_gradient_definition_passes_the_pins():
+    from tests.test_oracle_bwd_pins import pins_pass
+    assert pins_pass(lambda *a: _bwd_definition(*a))
+
+
+@pytest.mark.parametrize("mutation", ["mask_ignored", "dv_untransposed", "rowsum_over_keys_axis",
+                                      "dropped_rowsum", "sign_flip", "dq_transposed",
+                                      "dk_unscaled", "dk_uses_k"])
+def test_gradient_mutant_is_rejected(mutation):
+    from tests.test_oracle_bwd_pins import pins_pass
+    assert not pins_pass(lambda *a: _bwd_definition(*a, mutation=mutation))
