@@ -1,4 +1,5 @@
-"""GB300 (sm_103a) exact attention forward: Python binding of ``include/fa.h``.
+"""GB300 (sm_103a) exact attention, forward and backward: Python binding of
+``include/fa.h``.
 
 The binding only marshals arguments; every step of the computation runs in
 the CUDA kernels of ``libfa_gb300.so``.  PyTorch is used for device memory and
@@ -9,6 +10,11 @@ device is not sm_103, calls raise.
 
 q, k, v: CUDA bf16 tensors [B, H, L, d] (contiguous), d in {64, 128}.
 Returns o (bf16, same shape) and lse (fp32 [B, H, L], natural log).
+
+    dq, dk, dv = backward(q, k, v, o, lse, do, scale=None, causal=False)
+
+takes the forward's o and lse and the output gradient do (bf16, shaped like
+q) and returns the bf16 input gradients.
 """
 
 from __future__ import annotations
@@ -25,8 +31,9 @@ __all__ = [
     "library", "fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_static", "FA_STATIC_WORKSPACE_BYTES",
     "fa_splitkv_workspace_bytes", "fa_device_status",
     "fa_set_wait_timeout_ns", "fa_test_withhold_q_load", "fa_status_string", "fa_version",
-    "forward", "forward_splitkv",
-    "flops",
+    "fa_bwd", "fa_bwd_workspace_bytes",
+    "forward", "forward_splitkv", "backward",
+    "flops", "flops_bwd",
 ]
 
 FA_OK = 0
@@ -76,6 +83,11 @@ def library() -> ctypes.CDLL:
         lib.fa_test_withhold_q_load.restype = None
         lib.fa_status_string.argtypes = [ci]
         lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci,
+                               ctypes.c_float, ci, vp, ctypes.c_size_t, vp]
+        lib.fa_bwd.restype = ci
+        lib.fa_bwd_workspace_bytes.argtypes = [ci, ci, ci, ci]
+        lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_version.argtypes = []
         lib.fa_version.restype = ci
         _lib = lib
@@ -110,6 +122,17 @@ def fa_splitkv_workspace_bytes(B, H, L, d, n_splits) -> int:
     return library().fa_splitkv_workspace_bytes(B, H, L, d, n_splits)
 
 
+def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, L, d, scale, causal, workspace,
+           workspace_bytes, stream) -> int:
+    """Direct call of the backward C entry point with integer addresses."""
+    return library().fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, L, d, scale, causal,
+                            workspace, workspace_bytes, stream)
+
+
+def fa_bwd_workspace_bytes(B, H, L, d) -> int:
+    return library().fa_bwd_workspace_bytes(B, H, L, d)
+
+
 def fa_device_status(stream=None, clear=True) -> int:
     return library().fa_device_status(stream, int(bool(clear)))
 
@@ -135,6 +158,13 @@ def fa_version() -> int:
 def flops(B, H, L, d, causal) -> float:
     """Forward FLOPs by the metric's convention: 4*B*H*L^2*d, halved if causal."""
     f = 4.0 * B * H * L * L * d
+    return f / 2 if causal else f
+
+
+def flops_bwd(B, H, L, d, causal) -> float:
+    """Backward FLOPs by the usual convention: five L x L x d products,
+    10*B*H*L^2*d (2.5 x the forward), halved if causal."""
+    f = 10.0 * B * H * L * L * d
     return f / 2 if causal else f
 
 
@@ -209,3 +239,47 @@ def forward_splitkv(q, k, v, n_splits, scale=None, causal=False, out=None, lse=N
     if rc != FA_OK:
         raise FAError(rc, "fa_fwd_splitkv")
     return out, lse
+
+
+def backward(q, k, v, o, lse, do, scale=None, causal=False, dq=None, dk=None, dv=None,
+             workspace=None, stream=None):
+    """Gradients of exact attention: returns (dq, dk, dv), bf16 like q.
+
+    q, k, v, o, do: contiguous CUDA bf16 [B, H, L, d]; lse: fp32 [B, H, L]
+    from :func:`forward` with the same ``scale`` and ``causal``.
+    ``workspace`` (CUDA uint8, >= ``fa_bwd_workspace_bytes(B, H, L, d)``
+    bytes, 256-byte aligned) is allocated here when not given.
+    """
+    import torch
+
+    if not (q.shape == k.shape == v.shape == o.shape == do.shape) or q.dim() != 4:
+        raise ValueError("q, k, v, o, do must share one shape [B, H, L, d]")
+    for t in (q, k, v, o, do):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v, o, do must be contiguous CUDA bfloat16 tensors")
+    B, H, L, d = q.shape
+    if lse.shape != (B, H, L) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B, H, L]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = fa_bwd_workspace_bytes(B, H, L, d)
+    if need == 0:
+        raise ValueError("invalid sizes for the backward pass")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for t in (dq, dk, dv):
+        if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("dq, dk, dv must be contiguous bf16 tensors shaped like q")
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        rc = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                    lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, L, d,
+                    float(scale), int(bool(causal)), workspace.data_ptr(),
+                    workspace.numel() * workspace.element_size(), stream.cuda_stream)
+    if rc != FA_OK:
+        raise FAError(rc, "fa_bwd")
+    return dq, dk, dv

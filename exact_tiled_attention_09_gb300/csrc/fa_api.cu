@@ -1,5 +1,6 @@
 // Host side of the C ABI declared in include/fa.h: argument validation,
-// tensor-map encoding, kernel selection and launch.
+// tensor-map encoding, kernel selection and launch, for the forward pass
+// (single pass and split-KV) and the backward pass.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -9,6 +10,7 @@
 #include <mutex>
 
 #include "fa.h"
+#include "fa_bwd_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
 #include "fa_merge.cuh"
 
@@ -181,6 +183,45 @@ size_t workspace_bytes(int64_t BH, int L, int d, int n_splits) {
          static_cast<size_t>(n_splits) * rows * 4;
 }
 
+// ---------------------------------------------------------------- backward
+// Workspace of the backward pass: fp32 dQ accumulator [BH, L, d], then the
+// per-query terms -lse*log2(e) and -scale*<dO_i, O_i>, each [BH, Lp] with
+// Lp = L rounded up to 128, every part 256-byte aligned.
+struct BwdLayout {
+  size_t acc_bytes, row_bytes, total;
+};
+
+BwdLayout bwd_layout(int64_t BH, int L, int d) {
+  const size_t Lp = (static_cast<size_t>(L) + 127) / 128 * 128;
+  BwdLayout w;
+  w.acc_bytes = align256(static_cast<size_t>(BH) * static_cast<size_t>(L) * d * 4);
+  w.row_bytes = align256(static_cast<size_t>(BH) * Lp * 4);
+  w.total = w.acc_bytes + 2 * w.row_bytes;
+  return w;
+}
+
+template <int D, bool CAUSAL>
+int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+               const CUtensorMap& mdo, const BwdArgs& args, const BwdPreArgs& pre,
+               uint16_t* dq, cudaStream_t stream, int dev) {
+  auto kernel = fa_bwd_kernel<D, CAUSAL>;
+  constexpr int smem = BwdCfg<D>::SMEM_BYTES;
+  static bool configured[kMaxDevices] = {};
+  static std::mutex mu;
+  if (!configure_once(kernel, smem, dev, configured, mu)) return FA_ERR_LAUNCH;
+  const dim3 pre_grid(static_cast<unsigned>((pre.rows + BWD_AUX_WARPS - 1) / BWD_AUX_WARPS));
+  fa_bwd_pre_kernel<D><<<pre_grid, BWD_AUX_WARPS * 32, 0, stream>>>(pre);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  const dim3 grid(static_cast<unsigned>(args.bh) * static_cast<unsigned>(args.n_kv));
+  kernel<<<grid, BWD_THREADS, smem, stream>>>(mq, mk, mv, mdo, args);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  const long long n4 = static_cast<long long>(args.bh) * args.L * D / 4;
+  const long long blocks = (n4 + 255) / 256;
+  const dim3 post_grid(static_cast<unsigned>(blocks < 152 * 16 ? blocks : 152 * 16));
+  fa_bwd_post_kernel<<<post_grid, 256, 0, stream>>>(args.dq_acc, dq, n4);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
 }  // namespace
 }  // namespace fa
 
@@ -293,6 +334,100 @@ int fa_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o, 
                         FA_STATIC_WORKSPACE_BYTES, stream);
 }
 
+size_t fa_bwd_workspace_bytes(int B, int H, int L, int d) {
+  if (B < 1 || H < 1 || L < 1 || (d != 64 && d != 128)) return 0;
+  return fa::bwd_layout(static_cast<int64_t>(B) * H, L, d).total;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv, int B, int H, int L, int d, float scale,
+           int causal, void* workspace, size_t workspace_bytes_given, fa_stream_t stream) {
+  using namespace fa;
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
+    return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || L < 1) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  const int64_t n_kv = (static_cast<int64_t>(L) + 127) / 128;
+  if (BH > 0x7fffffff || BH * n_kv > 0x7fffffff ||
+      (BH * n_kv * 128 + BWD_AUX_WARPS - 1) / BWD_AUX_WARPS > 0x7fffffff)
+    return FA_ERR_INVALID_ARG;
+  const BwdLayout w = bwd_layout(BH, L, d);
+  if (workspace_bytes_given < w.total) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(lse, 4) || !aligned(workspace, 256))
+    return FA_ERR_MISALIGNED;
+
+  int dev = -1, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_DEVICE;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return FA_ERR_DEVICE;
+  if (major != 10 || minor != 3) return FA_ERR_DEVICE;
+
+  CUtensorMap mq, mk, mv, mdo;
+  if (!encode_map(&mq, q, static_cast<int>(BH), L, d) ||
+      !encode_map(&mk, k, static_cast<int>(BH), L, d) ||
+      !encode_map(&mv, v, static_cast<int>(BH), L, d) ||
+      !encode_map(&mdo, dout, static_cast<int>(BH), L, d))
+    return FA_ERR_LAUNCH;
+  unsigned int* status = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_status) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+
+  char* ws = static_cast<char*>(workspace);
+  float* acc = reinterpret_cast<float*>(ws);
+  float* nlse2 = reinterpret_cast<float*>(ws + w.acc_bytes);
+  float* nds = reinterpret_cast<float*>(ws + w.acc_bytes + w.row_bytes);
+  const int Lp = static_cast<int>(n_kv * 128);
+
+  BwdArgs args;
+  args.dk = static_cast<uint16_t*>(dk);
+  args.dv = static_cast<uint16_t*>(dv);
+  args.dq_acc = acc;
+  args.nlse2 = nlse2;
+  args.nds = nds;
+  args.L = L;
+  args.Lp = Lp;
+  args.n_kv = static_cast<int>(n_kv);
+  args.bh = static_cast<int>(BH);
+  {
+    // Heads per scheduling group: Q + dO (bf16) and the fp32 dQ accumulator
+    // of a group within ~32 MB of L2.
+    const int64_t head_bytes = static_cast<int64_t>(L) * d * 8;
+    const int64_t g = (int64_t{32} << 20) / head_bytes;
+    args.group_heads = static_cast<int>(g < 1 ? 1 : (g > BH ? BH : g));
+  }
+  args.scale_log2 = scale * 1.4426950408889634f;
+  args.scale = scale;
+  args.status = status;
+  args.timeout_ns = g_timeout_ns;
+  args.test_withhold_kv = g_test_withhold_q;
+
+  BwdPreArgs pre;
+  pre.o = static_cast<const uint16_t*>(o);
+  pre.dout = static_cast<const uint16_t*>(dout);
+  pre.lse = lse;
+  pre.nlse2 = nlse2;
+  pre.nds = nds;
+  pre.dq_acc = acc;
+  pre.L = L;
+  pre.Lp = Lp;
+  pre.rows = BH * Lp;
+  pre.scale = scale;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint16_t* dq16 = static_cast<uint16_t*>(dq);
+  if (d == 64)
+    return causal ? launch_bwd<64, true>(mq, mk, mv, mdo, args, pre, dq16, s, dev)
+                  : launch_bwd<64, false>(mq, mk, mv, mdo, args, pre, dq16, s, dev);
+  return causal ? launch_bwd<128, true>(mq, mk, mv, mdo, args, pre, dq16, s, dev)
+                : launch_bwd<128, false>(mq, mk, mv, mdo, args, pre, dq16, s, dev);
+}
+
 int fa_device_status(fa_stream_t stream, int clear) {
   using namespace fa;
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -323,6 +458,6 @@ const char* fa_status_string(int status) {
   }
 }
 
-int fa_version(void) { return 100; }
+int fa_version(void) { return 200; }
 
 }  // extern "C"

@@ -1,0 +1,574 @@
+// Exact attention backward for sm_103a: recomputation of P from Q, K and the
+// forward log-sum-exp, TMA + tcgen05 + TMEM, fp32 gradients accumulated on
+// chip.
+//
+// The gradients are those of "FlashAttention 深度解析", first part, section
+// 4.1 (dV = P^T dO, dP = dO V^T, dS = P (.) (dP - rowsum(dP (.) P))) with the
+// chain rule through the scaled scores S = scale * Q K^T (dQ = scale * dS K,
+// dK = scale * dS^T Q); P is recomputed block by block from the stored
+// per-row log-sum-exp instead of being read back (section 4.2, 重计算策略).
+// The row sum rowsum(dP (.) P)_i equals <dO_i, O_i> (dP = dO V^T and O = P V),
+// which a pre-pass computes once per query row from O and dO.
+//
+// Work unit: one CTA owns one block of 128 keys of one (batch, head), keeps
+// K_j and V_j in shared memory and dK_j, dV_j in tensor memory, and walks
+// the query blocks i (all of them, or i >= j with the causal mask).  Per
+// query block it computes, transposed so that its own keys are the TMEM
+// lanes:
+//
+//   S^T  = K_j Q_i^T                (SS MMA, M = keys, N = queries, K = d)
+//   dP^T = V_j dO_i^T               (SS MMA)
+//   P^T  = exp2(S^T * scale*log2e - lse_i*log2e)     (gradient warps)
+//   dV_j += P^T dO_i                (TS MMA: P^T from TMEM, bf16 over S^T)
+//   dS^T = scale * P^T (.) (dP^T - D_i)               (gradient warps, bf16
+//                                                      into shared memory)
+//   dK_j += dS^T Q_i                (SS MMA, dS^T K-major)
+//   dQ_i  = dS K_j                  (SS MMA, the same dS tile read MN-major,
+//                                    into the dP^T columns)
+//
+// and the gradient warps add dQ_i into an fp32 accumulator in global memory
+// (vector atomics; every key block of the head contributes to every dQ_i).
+// Post-pass: dQ = bf16(accumulator).
+//
+// Warp roles (320 threads):
+//   warp 0      MMA issuer, owner of the tensor memory (whole warp polls,
+//               one elected lane issues)
+//   warp 1      TMA producer: K_j, V_j once; Q_i and dO_i into a two-stage
+//               ring (full/empty mbarriers)
+//   warps 2..9  gradient warps: warp w handles TMEM lanes 32*(w%4)..+31
+//               (its keys) and query columns 64*h..64*h+63, h = (w-2)/4
+//
+// Tensor memory (512 columns): [0,128) S^T, then P^T as packed bf16 (half
+// h's 64 queries in columns 64h..64h+31); [128,256) dP^T, then dQ_i;
+// [256,256+D) dV_j; [256+D,256+2D) dK_j.
+//
+// Order of the MMAs per query block (tcgen05 operations of one thread
+// complete in issue order, which the hand-offs rely on):
+//   dP_i | wait P ready: dV_i | wait dS ready: dK_i, dQ_i | S_{i+1}
+// S_{i+1} overwrites P^T_i only after dV_i has read it; the commit that
+// publishes S_{i+1} also proves dK_i and dQ_i have read the dS tile, so the
+// gradient warps may overwrite it; dP_{i+1} waits until the gradient warps
+// have copied dQ_i out of its columns.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+constexpr int BWD_THREADS = 320;
+constexpr int BWD_STAGES = 2;
+constexpr int BWD_FIRST_GRAD_WARP = 2;
+constexpr int BWD_DS_BYTES = 128 * 128 * 2;  // dS^T tile, two 128 x 64 boxes
+
+// Wait sites of the backward kernel (bit index in the device status word).
+enum : uint32_t {
+  SITE_B_KV = 8,
+  SITE_B_FULL = 9,
+  SITE_B_EMPTY = 10,
+  SITE_B_S = 11,
+  SITE_B_DP = 12,
+  SITE_B_P = 13,
+  SITE_B_DS = 14,
+  SITE_B_DQ = 15,
+  SITE_B_DQFREE = 16,
+};
+
+template <int D>
+struct BwdCfg {
+  static_assert(D == 64 || D == 128, "head dimension must be 64 or 128");
+  static constexpr int BOXES = D / 64;
+  static constexpr int TILE_BYTES = 128 * D * 2;
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = TILE_BYTES;
+  static constexpr int STAGE_OFF = 2 * TILE_BYTES;      // stage s: Q at +0, dO at +TILE
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+  static constexpr int DS_OFF = STAGE_OFF + BWD_STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFF = DS_OFF + BWD_DS_BYTES;
+  // kv_full, full[S], empty[S], s_full, dp_full, p_ready, ds_ready, dq_full,
+  // dq_free, drain
+  static constexpr int NBAR = 1 + 2 * BWD_STAGES + 7;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + alignment slack
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static constexpr uint32_t S_COL = 0;
+  static constexpr uint32_t DP_COL = 128;
+  static constexpr uint32_t DV_COL = 256;
+  static constexpr uint32_t DK_COL = 256 + D;
+};
+
+struct BwdArgs {
+  uint16_t* dk;            // bf16 [BH, L, D]
+  uint16_t* dv;            // bf16 [BH, L, D]
+  float* dq_acc;           // fp32 [BH, L, D], zeroed by the pre-pass
+  const float* nlse2;      // fp32 [BH, Lp]: -lse * log2(e); -inf past L
+  const float* nds;        // fp32 [BH, Lp]: -scale * <dO_i, O_i>; 0 past L
+  int L;
+  int Lp;                  // L rounded up to a multiple of 128
+  int n_kv;                // key blocks per head = Lp / 128
+  int bh;                  // B * H
+  int group_heads;         // heads per scheduling group (see the CTA order)
+  float scale_log2;        // scale * log2(e)
+  float scale;
+  unsigned int* status;
+  unsigned long long timeout_ns;
+  int test_withhold_kv;    // test hook: skip the K/V copy so the first wait runs out
+};
+
+// Pre-pass arguments: per query row, the two per-row terms the main kernel
+// needs, and the zeroed dQ accumulator.
+struct BwdPreArgs {
+  const uint16_t* o;       // bf16 [BH, L, D]
+  const uint16_t* dout;    // bf16 [BH, L, D]
+  const float* lse;        // fp32 [BH, L]
+  float* nlse2;            // fp32 [BH, Lp]
+  float* nds;              // fp32 [BH, Lp]
+  float* dq_acc;           // fp32 [BH, L, D]
+  int L;
+  int Lp;
+  long long rows;          // BH * Lp
+  float scale;
+};
+
+constexpr int BWD_AUX_WARPS = 8;  // rows per block of the pre-pass
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Pre-pass, one warp per row of [BH, Lp]: D_i = <dO_i, O_i> (fp32, bf16
+// inputs), stored as -scale * D_i, and -lse_i * log2(e); rows past L get
+// the values that make them vanish in the main kernel (P = 0, dS = 0).  It
+// also zeroes the dQ accumulator row.
+template <int D>
+__global__ void __launch_bounds__(BWD_AUX_WARPS * 32) fa_bwd_pre_kernel(const BwdPreArgs a) {
+  const long long row = static_cast<long long>(blockIdx.x) * BWD_AUX_WARPS + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= a.rows) return;
+  const long long bh = row / a.Lp;
+  const int q = static_cast<int>(row - bh * a.Lp);
+  if (q >= a.L) {
+    if (lane == 0) {
+      a.nlse2[row] = -INFINITY;
+      a.nds[row] = 0.f;
+    }
+    return;
+  }
+  const size_t src = (static_cast<size_t>(bh) * a.L + q) * D;
+  float acc;
+  if constexpr (D == 64) {
+    const uint32_t ow = reinterpret_cast<const uint32_t*>(a.o + src)[lane];
+    const uint32_t dw = reinterpret_cast<const uint32_t*>(a.dout + src)[lane];
+    acc = fmaf(bf16_hi(ow), bf16_hi(dw), bf16_lo(ow) * bf16_lo(dw));
+    reinterpret_cast<float2*>(a.dq_acc + src)[lane] = make_float2(0.f, 0.f);
+  } else {
+    const uint2 ow = reinterpret_cast<const uint2*>(a.o + src)[lane];
+    const uint2 dw = reinterpret_cast<const uint2*>(a.dout + src)[lane];
+    acc = bf16_lo(ow.x) * bf16_lo(dw.x);
+    acc = fmaf(bf16_hi(ow.x), bf16_hi(dw.x), acc);
+    acc = fmaf(bf16_lo(ow.y), bf16_lo(dw.y), acc);
+    acc = fmaf(bf16_hi(ow.y), bf16_hi(dw.y), acc);
+    reinterpret_cast<float4*>(a.dq_acc + src)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) {
+    a.nlse2[row] = -a.lse[static_cast<size_t>(bh) * a.L + q] * 1.4426950408889634f;
+    a.nds[row] = -a.scale * acc;
+  }
+}
+
+// Post-pass: dQ = bf16(accumulator), four elements per thread and step.
+__global__ void __launch_bounds__(256) fa_bwd_post_kernel(const float* __restrict__ acc,
+                                                          uint16_t* __restrict__ dq,
+                                                          long long n4) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += stride) {
+    const float4 v = reinterpret_cast<const float4*>(acc)[i];
+    reinterpret_cast<uint2*>(dq)[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+  }
+}
+
+// Main backward kernel: one CTA per (head, key block); see the file comment.
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(BWD_THREADS, 1)
+    fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                  const BwdArgs args) {
+  using C = BwdCfg<D>;
+  constexpr uint32_t BOX = 128 * 64 * 2;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const base_ptr = smem_raw + (base - raw);
+
+  const uint32_t sK = base + C::K_OFF;
+  const uint32_t sV = base + C::V_OFF;
+  auto sQ = [&](int st) { return base + C::STAGE_OFF + st * C::STAGE_BYTES; };
+  auto sdO = [&](int st) { return base + C::STAGE_OFF + st * C::STAGE_BYTES + C::TILE_BYTES; };
+  const uint32_t sDS = base + C::DS_OFF;
+  uint8_t* const ds_ptr = base_ptr + C::DS_OFF;
+  const uint32_t bars = base + C::BAR_OFF;
+  const uint32_t bar_kv = bars;
+  auto bar_full = [&](int s) { return bars + 8u * (1 + s); };
+  auto bar_empty = [&](int s) { return bars + 8u * (1 + BWD_STAGES + s); };
+  const uint32_t bar_s = bars + 8u * (1 + 2 * BWD_STAGES);
+  const uint32_t bar_dp = bar_s + 8;
+  const uint32_t bar_p = bar_s + 16;
+  const uint32_t bar_ds = bar_s + 24;
+  const uint32_t bar_dq = bar_s + 32;
+  const uint32_t bar_dqfree = bar_s + 40;
+  const uint32_t bar_drain = bar_s + 48;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + C::MISC_OFF);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::MISC_OFF + 4);
+
+  const int warp = warp_index_uniform();
+  const int lane = threadIdx.x & 31;
+  const int L = args.L;
+  const int n_kv = args.n_kv;
+
+  // CTA order.  Heads go in groups of `group_heads` whose Q, dO and dQ
+  // accumulator fit comfortably in L2 (every key block of a head re-reads
+  // them).  Non-causal CTAs all cost the same and go head-major; causal key
+  // block j visits n_kv - j query blocks, so within a group block 0 of every
+  // head goes first (longest first).
+  const int BH = args.bh;
+  const int G = args.group_heads;
+  const int idx = static_cast<int>(blockIdx.x);
+  const int g0 = (idx / (G * n_kv)) * G;
+  const int gsz = min(G, BH - g0);
+  const int rk = idx - g0 * n_kv;
+  const int bh = CAUSAL ? g0 + rk % gsz : g0 + rk / n_kv;
+  const int jblk = CAUSAL ? rk / gsz : rk % n_kv;
+  const int q_first = CAUSAL ? jblk : 0;
+  const int n_i = n_kv - q_first;  // query blocks visited, >= 1
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_kv, 1);
+    for (int s = 0; s < BWD_STAGES; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    mbar_init(bar_s, 1);
+    mbar_init(bar_dp, 1);
+    mbar_init(bar_p, 8);  // one arrival per gradient warp
+    mbar_init(bar_ds, 8);
+    mbar_init(bar_dq, 1);
+    mbar_init(bar_dqfree, 8);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 1 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmdO);
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl ctl{abort_flag, args.status, args.timeout_ns};
+  auto warp_wait = [&](uint32_t bar, uint32_t parity, uint32_t site) -> bool {
+    const bool w = mbar_wait(bar, parity, ctl, site);
+    return __all_sync(0xffffffffu, w);
+  };
+
+  if (warp == 1) {
+    // ------------------------------------------------------------ producer
+    if (!args.test_withhold_kv && elect_one()) {
+      mbar_arrive_expect_tx(bar_kv, 2 * C::TILE_BYTES);
+      for (int c = 0; c < C::BOXES; ++c) {
+        tma_load_3d(sK + c * BOX, &tmK, bar_kv, c * 64, jblk * 128, bh);
+        tma_load_3d(sV + c * BOX, &tmV, bar_kv, c * 64, jblk * 128, bh);
+      }
+    }
+    __syncwarp();
+    int issued = 0;
+    bool ok = true;
+    for (; issued < n_i; ++issued) {
+      const int st = issued % BWD_STAGES;
+      const uint32_t use = static_cast<uint32_t>(issued / BWD_STAGES);
+      if (!warp_wait(bar_empty(st), (use & 1u) ^ 1u, SITE_B_EMPTY)) {
+        ok = false;
+        break;
+      }
+      if (elect_one()) {
+        mbar_arrive_expect_tx(bar_full(st), 2 * C::TILE_BYTES);
+        const int row = (q_first + issued) * 128;
+        for (int c = 0; c < C::BOXES; ++c) {
+          tma_load_3d(sQ(st) + c * BOX, &tmQ, bar_full(st), c * 64, row, bh);
+          tma_load_3d(sdO(st) + c * BOX, &tmdO, bar_full(st), c * 64, row, bh);
+        }
+      }
+      __syncwarp();
+    }
+    if (!ok && lane == 0) {
+      // Let every copy already issued land before the CTA exits.
+      if (!args.test_withhold_kv) mbar_wait_drain(bar_kv, 0, args.timeout_ns);
+      for (int s = 0; s < BWD_STAGES; ++s) {
+        const int n = issued > s ? (issued - 1 - s) / BWD_STAGES + 1 : 0;
+        if (n > 0) mbar_wait_drain(bar_full(s), (n - 1) & 1, args.timeout_ns);
+      }
+    }
+  } else if (warp == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t ID_S = idesc_bf16_f32_ab(128, 128, false, false);
+    constexpr uint32_t ID_DV = idesc_bf16_f32_ab(128, D, false, true);
+    constexpr uint32_t ID_DK = idesc_bf16_f32_ab(128, D, false, true);
+    constexpr uint32_t ID_DQ = idesc_bf16_f32_ab(128, D, true, true);
+    // scores-like products: A and B K-major tiles of this CTA, K = d
+    auto issue_kmajor = [&](uint32_t dcol, uint32_t a, uint32_t b, uint32_t bar) {
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * BOX + (kk & 3) * 32;
+          mma_ss(tmem + dcol, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(b + off, 16, 1024), ID_S,
+                 kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar);
+      }
+      __syncwarp();
+    };
+    bool ok = warp_wait(bar_kv, 0, SITE_B_KV);
+    if (ok) ok = warp_wait(bar_full(0), 0, SITE_B_FULL);
+    if (ok) {
+      tc_fence_after();
+      issue_kmajor(C::S_COL, sK, sQ(0), bar_s);
+    }
+    for (int i = 0; i < n_i && ok; ++i) {
+      const int st = i % BWD_STAGES;
+      if (i > 0) {
+        ok = warp_wait(bar_dqfree, (i - 1) & 1, SITE_B_DQFREE);
+        if (!ok) break;
+        tc_fence_after();
+      }
+      issue_kmajor(C::DP_COL, sV, sdO(st), bar_dp);
+      // dV += P^T dO_i once the gradient warps have written P^T.
+      ok = warp_wait(bar_p, i & 1, SITE_B_P);
+      if (!ok) break;
+      tc_fence_after();
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + C::DV_COL, tmem + C::S_COL + 64 * (kk >> 2) + 8 * (kk & 3),
+                 sdesc_sw128(sdO(st) + kk * 2048, BOX, 1024), ID_DV, (i > 0 || kk > 0) ? 1u : 0u);
+      }
+      __syncwarp();
+      // dK += dS^T Q_i and dQ_i = dS K_j once dS^T is in shared memory.
+      ok = warp_wait(bar_ds, i & 1, SITE_B_DS);
+      if (!ok) break;
+      tc_fence_after();
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + C::DK_COL, sdesc_sw128(sDS + (kk >> 2) * BOX + (kk & 3) * 32, 16, 1024),
+                 sdesc_sw128(sQ(st) + kk * 2048, BOX, 1024), ID_DK, (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + C::DP_COL, sdesc_sw128(sDS + kk * 2048, BOX, 1024),
+                 sdesc_sw128(sK + kk * 2048, BOX, 1024), ID_DQ, kk > 0 ? 1u : 0u);
+        mma_commit(bar_dq);
+        mma_commit(bar_empty(st));
+      }
+      __syncwarp();
+      if (i + 1 < n_i) {
+        const int st2 = (i + 1) % BWD_STAGES;
+        ok = warp_wait(bar_full(st2), static_cast<uint32_t>((i + 1) / BWD_STAGES) & 1u,
+                       SITE_B_FULL);
+        if (!ok) break;
+        tc_fence_after();
+        issue_kmajor(C::S_COL, sK, sQ(st2), bar_s);
+      }
+    }
+    if (!ok) {
+      // Every MMA already issued must finish before the tensor memory is freed.
+      if (elect_one()) {
+        mma_commit(bar_drain);
+        mbar_wait_drain(bar_drain, 0, args.timeout_ns);
+      }
+      __syncwarp();
+    }
+  } else {
+    // ------------------------------------------------------------ gradient warps
+    const int h = (warp - BWD_FIRST_GRAD_WARP) >> 2;  // query half: columns 64h..64h+63
+    const int quarter = warp & 3;                      // TMEM lanes this warp may access
+    const int r = quarter * 32 + lane;                 // TMEM lane: key row (S^T, dP^T,
+                                                       // dK, dV) or query row (dQ)
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const int key = jblk * 128 + r;
+    const bool key_ok = key < L;
+    const uint64_t sl2x2 = f2_pack(args.scale_log2, args.scale_log2);
+    const uint64_t scale2 = f2_pack(args.scale, args.scale);
+    const float* const nlse_head = args.nlse2 + static_cast<size_t>(bh) * args.Lp;
+    const float* const nds_head = args.nds + static_cast<size_t>(bh) * args.Lp;
+    bool ok = true;
+
+    for (int i = 0; i < n_i; ++i) {
+      const int qb = q_first + i;
+      const int qh0 = qb * 128 + 64 * h;  // first query of this warp's half
+      const bool diag = CAUSAL && qb == jblk;
+
+      // P^T = exp2(S^T * scale*log2e - lse*log2e), kept in fp32 for dS and
+      // written to TMEM as bf16 (the A operand of dV += P^T dO).
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_s, i & 1, ctl, SITE_B_S))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float p[64];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t sr[32];
+        tmem_ld32(lane_base + C::S_COL + 64 * h + 32 * c, sr);
+        tmem_wait_ld();
+        reg_fence32(sr);
+        const float4* nl = reinterpret_cast<const float4*>(nlse_head + qh0 + 32 * c);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 a = nl[e >> 2];
+          float x0, x1, x2, x3;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl2x2,
+                           f2_pack(a.x, a.y)),
+                    x0, x1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), sl2x2,
+                           f2_pack(a.z, a.w)),
+                    x2, x3);
+          float pe[4] = {ex2_approx(x0), ex2_approx(x1), ex2_approx(x2), ex2_approx(x3)};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            // causal: key r > query (64h + 32c + e + u) of the same block;
+            // keys past L (zero rows of K) never contribute.
+            if ((diag && r > 64 * h + 32 * c + e + u) || !key_ok) pe[u] = 0.f;
+            p[32 * c + e + u] = pe[u];
+          }
+          pk[e >> 1] = pack_bf16x2(pe[0], pe[1]);
+          pk[(e >> 1) + 1] = pack_bf16x2(pe[2], pe[3]);
+        }
+        tmem_st16(lane_base + C::S_COL + 64 * h + 16 * c, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_p);
+
+      // dS^T = P^T (.) (scale * dP^T - scale * D), bf16 into the 128B-swizzled
+      // dS tile: row = key, box h holds this half's 64 queries.
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_dp, i & 1, ctl, SITE_B_DP))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t dr[32];
+        tmem_ld32(lane_base + C::DP_COL + 64 * h + 32 * c, dr);
+        tmem_wait_ld();
+        reg_fence32(dr);
+        const float4* nd = reinterpret_cast<const float4*>(nds_head + qh0 + 32 * c);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 b = nd[e >> 2];
+          float d0, d1, d2, d3;
+          f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
+                                  scale2, f2_pack(b.x, b.y)),
+                           f2_pack(p[32 * c + e], p[32 * c + e + 1])),
+                    d0, d1);
+          f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(dr[e + 2]), __uint_as_float(dr[e + 3])),
+                                  scale2, f2_pack(b.z, b.w)),
+                           f2_pack(p[32 * c + e + 2], p[32 * c + e + 3])),
+                    d2, d3);
+          pk[e >> 1] = pack_bf16x2(d0, d1);
+          pk[(e >> 1) + 1] = pack_bf16x2(d2, d3);
+        }
+        uint8_t* const row_ptr = ds_ptr + h * BOX + r * 128;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int unit = (4 * c + u) ^ (r & 7);
+          *reinterpret_cast<uint4*>(row_ptr + unit * 16) =
+              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+      fence_proxy_async_smem();  // the MMA reads the tile through the async proxy
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_ds);
+
+      // dQ_i: copy this warp's D/2 columns out of TMEM, release the columns,
+      // then add them into the fp32 accumulator (row = query qb*128 + r).
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_dq, i & 1, ctl, SITE_B_DQ))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t qv[D / 64][32];
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) tmem_ld32(lane_base + C::DP_COL + (D / 2) * h + 32 * c, qv[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) reg_fence32(qv[c]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_dqfree);
+      const int qrow = qb * 128 + r;
+      if (qrow < L) {
+        float4* dst = reinterpret_cast<float4*>(
+            args.dq_acc + (static_cast<size_t>(bh) * L + qrow) * D + (D / 2) * h);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            atomicAdd(dst + 8 * c + (e >> 2),
+                      make_float4(__uint_as_float(qv[c][e]), __uint_as_float(qv[c][e + 1]),
+                                  __uint_as_float(qv[c][e + 2]), __uint_as_float(qv[c][e + 3])));
+      }
+    }
+
+    // Epilogue: the last dq_full arrival came after every MMA of the CTA, so
+    // dV_j and dK_j are final.  bf16 (round to nearest even), rows < L.
+    if (ok) {
+      const size_t row = static_cast<size_t>(bh) * L + key;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col0 = (which == 0 ? C::DV_COL : C::DK_COL) + (D / 2) * h;
+        uint16_t* const out = which == 0 ? args.dv : args.dk;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t v[32];
+          tmem_ld32(lane_base + col0 + 32 * c, v);
+          tmem_wait_ld();
+          reg_fence32(v);
+          if (key_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(out + row * D + (D / 2) * h + 32 * c);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              dst[u] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * u]), __uint_as_float(v[8 * u + 1])),
+                                  pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3])),
+                                  pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5])),
+                                  pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7])));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace fa

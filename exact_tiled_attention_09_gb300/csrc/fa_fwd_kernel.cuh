@@ -113,16 +113,6 @@ struct FwdArgs {
   int test_withhold_q;  // test hook: skip the Q copy so the first MMA wait runs out
 };
 
-// Wait that ignores the CTA abort flag (used while draining after an abort).
-__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity,
-                                                unsigned long long timeout_ns) {
-  const uint64_t t0 = global_timer_ns();
-  for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > timeout_ns) return false;
-  }
-}
-
 // Number of K/V blocks Q tile t of this CTA needs (0 if the tile lies wholly
 // past the end of the sequence).  Causal: blocks whose first key exceeds the
 // tile's last query are skipped.

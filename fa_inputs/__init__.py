@@ -17,7 +17,8 @@ Generator
   element ``2p + 1`` the sine branch.
 * Q, K and V are drawn in that order from ONE counter stream, element-major
   over ``[B, H, L, d]``: Q takes counters ``[0, n)``, K ``[n, 2n)``,
-  V ``[2n, 3n)`` where ``n = B*H*L*d``.
+  V ``[2n, 3n)`` where ``n = B*H*L*d``.  The output gradient dO of the
+  backward pass (standard deviation 1) takes ``[3n, 4n)``.
 * Each variate is multiplied by its tensor's standard deviation, rounded to
   float32 (round-to-nearest-even) and then to bfloat16 (round-to-nearest-
   even on the float32 bit pattern).
@@ -43,6 +44,9 @@ __all__ = [
     "bf16_bits_to_float32",
     "make_qkv",
     "make_qkv_rows",
+    "make_grad_out",
+    "make_grad_out_rows",
+    "make_custom_grad_out",
 ]
 
 _PHI = np.uint64(0x9E3779B97F4A7C15)
@@ -199,6 +203,26 @@ def make_qkv_rows(w: AttentionWorkload, bh: int, rows: np.ndarray):
         z = normal_at(w.seed, base + np.uint64(t * n))
         out.append(round_to_bf16_bits(std * z).reshape(rows.size, w.d))
     return tuple(out)
+
+
+def make_grad_out(w: AttentionWorkload):
+    """The output gradient dO (bf16 bits [B,H,L,d], standard normal)."""
+    n = w.n_elem
+    return _fill(w.seed, 3 * n, n, 1.0).reshape(w.B, w.H, w.L, w.d)
+
+
+def make_grad_out_rows(w: AttentionWorkload, bh: int, rows: np.ndarray):
+    """Rows ``rows`` of head ``bh`` of :func:`make_grad_out` ([len(rows), d])."""
+    n = w.n_elem
+    rows = np.asarray(rows, dtype=np.int64)
+    base = (bh * w.L + rows)[:, None] * w.d + np.arange(w.d, dtype=np.int64)[None, :]
+    z = normal_at(w.seed, base.astype(np.uint64) + np.uint64(3 * n))
+    return round_to_bf16_bits(z).reshape(rows.size, w.d)
+
+
+def make_custom_grad_out(B, H, L, d, seed):
+    """dO for an ad-hoc shape, from the same stream as :func:`make_custom`."""
+    return make_grad_out(AttentionWorkload("custom", B, H, L, d, False, 1.0, seed))
 
 
 def make_custom(B, H, L, d, seed, q_std=1.0, k_std=1.0, v_std=1.0):

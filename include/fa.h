@@ -1,5 +1,6 @@
 /*
- * fa.h -- C ABI of the GB300 (sm_103a) exact attention forward pass.
+ * fa.h -- C ABI of the GB300 (sm_103a) exact attention forward and backward
+ * passes.
  *
  * The operation is exact scaled-dot-product attention with the per-row
  * log-sum-exp, computed FlashAttention-style: tiles of Q stay on chip, K and
@@ -146,6 +147,53 @@ int fa_fwd_splitkv_static(const void *q, const void *k, const void *v, void *o, 
                           fa_stream_t stream);
 
 /*
+ * fa_bwd_workspace_bytes -- bytes of workspace fa_bwd needs for these sizes:
+ * 256-byte-aligned room for an fp32 dQ accumulator [B, H, L, d] and two fp32
+ * per-query arrays [B, H, Lp] (Lp = L rounded up to a multiple of 128).
+ * Returns 0 for invalid sizes (B/H/L < 1, d not 64/128).  Host only.
+ */
+size_t fa_bwd_workspace_bytes(int B, int H, int L, int d);
+
+/*
+ * fa_bwd -- gradients of exact attention (the backward pass by
+ * recomputation): given the forward's inputs, its outputs o and lse, and the
+ * gradient dout of a loss with respect to o, write the gradients with
+ * respect to q, k and v.
+ *
+ *   The formulas are those of "FlashAttention 深度解析", first part, section
+ *   4.1 (dV = P^T dO; dP = dO V^T; dS = P (.) (dP - rowsum(dP (.) P))) with
+ *   the chain rule through the scaled scores (dQ = scale dS K, dK = scale
+ *   dS^T Q).  P is recomputed block by block from q, k and lse, never stored
+ *   (section 4.2, 重计算策略); rowsum(dP (.) P) is computed as <dO_i, O_i>,
+ *   equal to it because O = P V.
+ *
+ *   q, k, v, o, dout : device bf16 [B, H, L, d], layout as for fa_fwd,
+ *               16-byte aligned; o is fa_fwd's output for q, k, v, scale,
+ *               causal.  Read only.
+ *   lse       : device fp32 [B, H, L], fa_fwd's log-sum-exp for the same
+ *               call; 4-byte aligned.  Read only.
+ *   dq, dk, dv: device bf16 [B, H, L, d], 16-byte aligned, fully overwritten
+ *               (round to nearest even from fp32 accumulators).
+ *   B..causal : as for fa_fwd (d = 64 or 128).
+ *   workspace : device scratch owned by the caller, 256-byte aligned, at
+ *               least fa_bwd_workspace_bytes(B, H, L, d) bytes; contents on
+ *               entry do not matter and are undefined after.
+ *
+ * The caller owns every buffer; dq, dk, dv and workspace must not overlap
+ * each other or the inputs.  Three kernels are launched on `stream` (a
+ * per-row pre-pass, the gradient kernel, a dQ conversion pass); calls that
+ * share a workspace on concurrent streams race.  Arithmetic: bf16 operands
+ * (P and dS rounded to bf16 before their products), fp32 accumulation, dQ
+ * summed over key blocks with fp32 atomic adds, so its last bits may differ
+ * from run to run.  Errors: those of fa_fwd, plus FA_ERR_INVALID_ARG for a
+ * null or too-small workspace and FA_ERR_MISALIGNED for a workspace that is
+ * not 256-byte aligned; nothing is launched on an error.
+ */
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+           const float *lse, void *dq, void *dk, void *dv, int B, int H, int L, int d,
+           float scale, int causal, void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
  * fa_device_status -- synchronise `stream` and report whether any kernel of
  * this library on the current device gave up a bounded wait since the status
  * was last cleared (FA_ERR_TIMEOUT) or FA_OK.  A nonzero `clear` resets the
@@ -164,11 +212,12 @@ void fa_set_wait_timeout_ns(uint64_t ns);
 
 /*
  * fa_test_withhold_q_load -- test hook for the timeout path.  While enabled
- * (nonzero), the attention kernels launched afterwards skip their Q copy, so
- * the MMA warp's first wait never completes: it gives up after the wait
- * limit, every role stops and drains, the tensor memory is freed and
- * fa_device_status reports FA_ERR_TIMEOUT.  Outputs of such launches are
- * undefined.  Process-wide; leave at 0 outside such tests.
+ * (nonzero), the forward kernels launched afterwards skip their Q copy and
+ * the backward kernel its K/V copy, so the MMA warp's first wait never
+ * completes: it gives up after the wait limit, every role stops and drains,
+ * the tensor memory is freed and fa_device_status reports FA_ERR_TIMEOUT.
+ * Outputs of such launches are undefined.  Process-wide; leave at 0 outside
+ * such tests.
  */
 void fa_test_withhold_q_load(int enable);
 

@@ -2,6 +2,8 @@
 
 from __future__ import annotations
 
+import math
+
 import numpy as np
 
 # Tolerances for bf16 inputs with fp32 accumulation against the fp64 oracle.
@@ -59,3 +61,49 @@ def check_parity(o_gpu, lse_gpu, o_ref, lse_ref, label=""):
     el = np.abs(lse_gpu - lse_ref).max()
     assert el <= LSE_MAX_ABS, f"{label}: max |dLSE| {el:.3e}"
     return float(err.max()), mean_err, float(el)
+
+
+# Gradients (backward pass).  Per head and per gradient tensor G, against the
+# exact fp64 gradient:
+#   max |G - G_ref|      <= GRAD_MAX_REL * max |G_ref| + GRAD_ATOL
+#   ||G - G_ref||_F      <= GRAD_FRO_REL * ||G_ref||_F + GRAD_ATOL * sqrt(n)
+# The kernel rounds P and dS to bf16 (unit roundoff u = 2^-9) before their
+# products and writes bf16 outputs (another u per element); D = <dO, O> uses
+# the bf16 forward output.  Emulating exactly those roundings on the CPU gives
+# normwise errors of 2.3e-3 (N(0,1) inputs) to 4.8e-3 (Q, K ~ N(0, 3^2)) and
+# worst elements at 6.7e-3 of max |G_ref|; the bounds are about 2x and 3x
+# those, i.e. about 5u normwise and 10u elementwise.  GRAD_ATOL covers
+# gradients that are exactly zero in fp64 (e.g. dQ, dK with one key) and come
+# out as fp32 rounding noise.
+GRAD_MAX_REL = 2e-2
+GRAD_FRO_REL = 1e-2
+GRAD_ATOL = 1e-4
+
+
+def check_grad(g_gpu, g_ref, label=""):
+    """Assert the gradient tolerances for one head's [rows, d] gradient;
+    return (max err / max |ref|, normwise relative error)."""
+    assert np.isfinite(g_gpu).all(), f"{label}: non-finite gradient"
+    err = np.abs(g_gpu - g_ref)
+    ref_max = float(np.abs(g_ref).max()) if g_ref.size else 0.0
+    bound = GRAD_MAX_REL * ref_max + GRAD_ATOL
+    assert err.max() <= bound, (f"{label}: max err {err.max():.3e} > {bound:.3e} "
+                                f"(max |ref| {ref_max:.3e})")
+    fro_ref = float(np.linalg.norm(g_ref))
+    fro_err = float(np.linalg.norm(err))
+    fbound = GRAD_FRO_REL * fro_ref + GRAD_ATOL * math.sqrt(err.size)
+    assert fro_err <= fbound, f"{label}: normwise err {fro_err:.3e} > {fbound:.3e}"
+    return (float(err.max()) / ref_max if ref_max else 0.0,
+            fro_err / fro_ref if fro_ref else 0.0)
+
+
+def check_grads_per_head(got, ref, label=""):
+    """got/ref: (dq, dk, dv) arrays [..., L, d]; checks every head."""
+    worst = {}
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        g = g.reshape(-1, g.shape[-2], g.shape[-1])
+        r = r.reshape(-1, r.shape[-2], r.shape[-1])
+        for h in range(g.shape[0]):
+            m, f = check_grad(g[h], r[h], f"{label} {name} head {h}")
+            worst[name] = max(worst.get(name, (0, 0))[0], m), max(worst.get(name, (0, 0))[1], f)
+    return worst

@@ -147,3 +147,70 @@ def test_splitkv_validation_launches_nothing(lib):
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
         assert _call_split() == fa.FA_ERR_DEVICE
+
+
+# ---------------------------------------------------------------- backward
+BWD_GOOD = dict(q=0x10000, k=0x20000, v=0x30000, o=0x40000, dout=0x50000, lse=0x60000,
+                dq=0x70000, dk=0x80000, dv=0x90000, B=1, H=2, L=300, d=64, scale=0.125,
+                causal=0, ws=0x1000000)
+
+
+def test_bwd_workspace_bytes(lib):
+    B, H, L, d = 2, 3, 300, 128
+    Lp = 384
+    acc = ((B * H * L * d * 4 + 255) // 256) * 256
+    row = ((B * H * Lp * 4 + 255) // 256) * 256
+    assert fa.fa_bwd_workspace_bytes(B, H, L, d) == acc + 2 * row
+    assert fa.fa_bwd_workspace_bytes(B, H, L, 96) == 0
+    assert fa.fa_bwd_workspace_bytes(0, H, L, d) == 0
+    assert fa.fa_bwd_workspace_bytes(B, H, 0, d) == 0
+
+
+def _call_bwd(ws_bytes=None, **over):
+    a = dict(BWD_GOOD)
+    a.update(over)
+    if ws_bytes is None:
+        ws_bytes = fa.fa_bwd_workspace_bytes(a["B"], a["H"], a["L"], a["d"]) or (1 << 30)
+    return fa.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["dout"], a["lse"], a["dq"], a["dk"],
+                     a["dv"], a["B"], a["H"], a["L"], a["d"], a["scale"], a["causal"], a["ws"],
+                     ws_bytes, None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=0), fa.FA_ERR_INVALID_ARG),
+    (dict(o=0), fa.FA_ERR_INVALID_ARG),
+    (dict(dout=0), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=0), fa.FA_ERR_INVALID_ARG),
+    (dict(dq=0), fa.FA_ERR_INVALID_ARG),
+    (dict(dk=0), fa.FA_ERR_INVALID_ARG),
+    (dict(dv=0), fa.FA_ERR_INVALID_ARG),
+    (dict(ws=0), fa.FA_ERR_INVALID_ARG),
+    (dict(ws_bytes=1000), fa.FA_ERR_INVALID_ARG),
+    (dict(L=0), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=3), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(B=1 << 16, H=1 << 16), fa.FA_ERR_INVALID_ARG),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED_D),
+    (dict(dout=0x50008), fa.FA_ERR_MISALIGNED),
+    (dict(dk=0x80002), fa.FA_ERR_MISALIGNED),
+    (dict(lse=0x60002), fa.FA_ERR_MISALIGNED),
+    (dict(ws=0x1000080), fa.FA_ERR_MISALIGNED),
+])
+def test_bwd_validation_errors_launch_nothing(lib, over, code):
+    assert _call_bwd(**over) == code
+
+
+def test_bwd_well_formed_call_without_gpu_reports_device_error(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; fake pointers must not reach a launch")
+    assert _call_bwd() == fa.FA_ERR_DEVICE
+    assert _call_bwd(d=128, causal=1) == fa.FA_ERR_DEVICE
+
+
+def test_python_backward_rejects_bad_tensors():
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    lse = torch.zeros(1, 1, 8)
+    with pytest.raises(ValueError):
+        fa.backward(q, q, q, q, lse, q)  # CPU tensors

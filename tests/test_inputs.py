@@ -77,3 +77,15 @@ def test_workload_table():
     assert w["B1_H32_L16384_d128_causal_qk3"].q_std == 3.0
     assert w["B1_H32_L16384_d128_causal_qk3"].v_std == 1.0
     assert [x.seed for x in w.values()] == [42, 43, 44, 45, 46, 47]
+
+
+def test_grad_out_follows_v_in_the_same_stream():
+    from fa_inputs import (AttentionWorkload, make_grad_out, make_grad_out_rows,
+                           normal_variates, round_to_bf16_bits)
+    w = AttentionWorkload("t", 2, 3, 50, 8, False, 1.0, 9)
+    do = make_grad_out(w)
+    n = w.n_elem
+    expect = round_to_bf16_bits(normal_variates(9, 3 * n, n)).reshape(do.shape)
+    assert np.array_equal(do, expect)
+    rows = np.array([0, 7, 49])
+    assert np.array_equal(make_grad_out_rows(w, 4, rows), do.reshape(6, 50, 8)[4][rows])

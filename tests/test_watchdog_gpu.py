@@ -78,3 +78,36 @@ def test_wait_that_runs_out_is_reported_and_the_context_survives(dev, d, causal,
     o_ref, lse_ref = oracle.attention(_f64(qb), _f64(kb), _f64(vb), scale, causal)
     check_parity(from_device(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
                  f"after timeout d={d} causal={causal} split={split}")
+
+
+@pytest.mark.parametrize("d,causal", [(64, False), (128, True)])
+def test_backward_wait_that_runs_out_is_reported(dev, d, causal):
+    import torch
+    from fa_inputs import make_custom_grad_out
+    B, H, L = 1, 2, 300
+    qb, kb, vb = make_custom(B, H, L, d, seed=710 + d)
+    dob = make_custom_grad_out(B, H, L, d, 710 + d)
+    q, k, v, do = (to_device(x, dev) for x in (qb, kb, vb, dob))
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.forward(q, k, v, scale=scale, causal=causal)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status(None, clear=True) == fa.FA_OK
+    try:
+        fa.fa_set_wait_timeout_ns(SHORT_LIMIT_NS)
+        fa.fa_test_withhold_q_load(True)  # the backward kernel skips its K/V copy
+        t0 = time.time()
+        fa.backward(q, k, v, o, lse, do, scale=scale, causal=causal)
+        torch.cuda.synchronize()
+        elapsed = time.time() - t0
+        status = fa.fa_device_status(None, clear=True)
+    finally:
+        fa.fa_test_withhold_q_load(False)
+        fa.fa_set_wait_timeout_ns(DEFAULT_LIMIT_NS)
+    assert status == fa.FA_ERR_TIMEOUT
+    assert elapsed < 10.0
+    dq, dk, dv = fa.backward(q, k, v, o, lse, do, scale=scale, causal=causal)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status(None, clear=True) == fa.FA_OK
+    ref = oracle.attention_bwd(_f64(qb), _f64(kb), _f64(vb), _f64(dob), scale, causal)
+    from tests.gpu_util import check_grads_per_head
+    check_grads_per_head([from_device(t) for t in (dq, dk, dv)], ref, "bwd after timeout")
