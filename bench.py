@@ -20,7 +20,9 @@ LSE back, all inside the timed events.
 seeded inputs), each timed the same way, including the d=128 non-causal
 L=8192 point used for the tensor-core fraction.  ``splitkv`` times the
 split-KV path (split pass + merge) against the single pass on shapes whose
-single-pass grid underfills the GPU.
+single-pass grid underfills the GPU.  ``backward`` times the backward pass
+(gradients by recomputation) on every workload: TFLOP/s by the convention
+10*B*H*L^2*d (five L x L x d products; halved when causal).
 
 With more than one GPU (torchrun) every rank runs its own replica of the
 workload (the forward pass has no exchange step); only the timing is
@@ -237,6 +239,44 @@ def time_splitkv(fa, torch, q, k, v, w, n_splits, steps, warmup, flush_buf):
     return [s_.elapsed_time(e_) for s_, e_ in ev]
 
 
+def time_backward(fa, torch, w, dev, steps, warmup, flush_buf):
+    """Per-step device time (ms) of ``fa.backward`` (row pre-pass, gradient
+    kernel, dQ conversion) on device-generated seeded inputs; O and LSE come
+    from the forward, dO is a seeded normal.  L2 flushed before each step."""
+    q, k, v = device_inputs(w, dev, torch)
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed + 1000)
+    do = torch.randn(q.shape, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    stream = torch.cuda.current_stream()
+    o, lse = fa.forward(q, k, v, scale=w.scale, causal=w.causal, stream=stream)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.L, w.d), dtype=torch.uint8,
+                     device=dev)
+    run = lambda: fa.backward(q, k, v, o, lse, do, scale=w.scale, causal=w.causal, dq=dq, dk=dk,
+                              dv=dv, workspace=ws, stream=stream)
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for s_, e_ in ev:
+        flush_buf.fill_(1)
+        s_.record(stream)
+        run()
+        e_.record(stream)
+    torch.cuda.synchronize()
+    return [s_.elapsed_time(e_) for s_, e_ in ev]
+
+
+def backward_line(fa, w, t, peaks):
+    mean = sum(t) / len(t)
+    f = fa.flops_bwd(w.B, w.H, w.L, w.d, w.causal)
+    tf = f / (mean * 1e-3) / 1e12
+    return {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d, "causal": w.causal,
+            "ms_mean": round(mean, 4), "ms_min": round(min(t), 4), "tflops": round(tf, 1),
+            "frac_of_peak": round(tf / peaks["bf16_tflops"], 4), "steps": len(t)}
+
+
 def splits_for(w, sms):
     """Smallest split count that fills one wave of CTAs (two when causal,
     whose CTAs differ in cost); at most one split per 128-key block and 64."""
@@ -333,6 +373,7 @@ def run_ours(args):
 
     extras = []
     splitkv = []
+    backward = []
     with ClockSampler(local) as clk:
         if world > 1:
             dist.barrier()
@@ -357,6 +398,11 @@ def run_ours(args):
                                "frac_of_peak": round(tf / peaks["bf16_tflops"], 4),
                                "steps": steps})
                 del qx, kx, vx
+            for name, wx in WORKLOADS.items():
+                steps = max(3, min(args.extra_steps,
+                                   int(5e13 / fa.flops_bwd(wx.B, wx.H, wx.L, wx.d, wx.causal))))
+                t = time_backward(fa, torch, wx, dev, steps, 3, flush_buf)
+                backward.append(backward_line(fa, wx, t, peaks))
             from fa_inputs import AttentionWorkload
             sms = torch.cuda.get_device_properties(dev).multi_processor_count
             for name, B, H, L, d, causal in SPLITKV_SHAPES:
@@ -425,11 +471,31 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "workloads": extras,
             "splitkv": splitkv,
+            "backward": backward,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def run_profile_bwd(args):
+    """Time only the backward pass of one workload (for profiler captures)."""
+    import torch
+
+    import exact_tiled_attention_09_gb300 as fa
+    from fa_inputs import WORKLOADS
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fa.library()
+    peaks, _ = read_peaks()
+    w = WORKLOADS[args.profile_bwd]
+    flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    t = time_backward(fa, torch, w, dev, args.steps, args.warmup, flush_buf)
+    if fa.fa_device_status(None, clear=True) != fa.FA_OK:
+        raise RuntimeError("a kernel wait timed out during the benchmark")
+    print(json.dumps({"backward": backward_line(fa, w, t, peaks)}), flush=True)
 
 
 def run_reference(args):
@@ -485,9 +551,14 @@ def main():
     ap.add_argument("--device-inputs", action="store_true",
                     help="draw the headline inputs with a seeded device generator "
                          "(no CPU baseline then); used for profiling large workloads")
+    ap.add_argument("--profile-bwd", metavar="WORKLOAD", default=None,
+                    help="time only the backward pass of WORKLOAD and print its line "
+                         "(for profiler captures; not the benchmark line)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
-    if args.impl == "reference":
+    if args.profile_bwd:
+        run_profile_bwd(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -62,6 +62,24 @@ bool encode_map(CUtensorMap* map, const void* ptr, int BH, int L, int D) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The fp32 dQ accumulator [BH, L, D] as a 3-D tensor (D, L, BH) with a
+// 32 x 32 x 1 box (128-byte rows) and the 128-byte swizzle: the target of
+// the backward kernel's reduce-adds.  Rows past L inside a head are out of
+// bounds, so a reduce of a ragged block never touches the next head.
+bool encode_map_f32_acc(CUtensorMap* map, void* ptr, int BH, int L, int D) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 4,
+                                 static_cast<cuuint64_t>(L) * D * 4};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <typename Kernel>
 bool configure_once(Kernel kernel, int smem, int dev, bool* configured, std::mutex& mu) {
   std::lock_guard<std::mutex> lock(mu);
@@ -202,8 +220,8 @@ BwdLayout bwd_layout(int64_t BH, int L, int d) {
 
 template <int D, bool CAUSAL>
 int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-               const CUtensorMap& mdo, const BwdArgs& args, const BwdPreArgs& pre,
-               uint16_t* dq, cudaStream_t stream, int dev) {
+               const CUtensorMap& mdo, const CUtensorMap& mdq, const BwdArgs& args,
+               const BwdPreArgs& pre, uint16_t* dq, cudaStream_t stream, int dev) {
   auto kernel = fa_bwd_kernel<D, CAUSAL>;
   constexpr int smem = BwdCfg<D>::SMEM_BYTES;
   static bool configured[kMaxDevices] = {};
@@ -213,7 +231,7 @@ int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
   fa_bwd_pre_kernel<D><<<pre_grid, BWD_AUX_WARPS * 32, 0, stream>>>(pre);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   const dim3 grid(static_cast<unsigned>(args.bh) * static_cast<unsigned>(args.n_kv));
-  kernel<<<grid, BWD_THREADS, smem, stream>>>(mq, mk, mv, mdo, args);
+  kernel<<<grid, BWD_THREADS, smem, stream>>>(mq, mk, mv, mdo, mdq, args);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   const long long n4 = static_cast<long long>(args.bh) * args.L * D / 4;
   const long long blocks = (n4 + 255) / 256;
@@ -380,6 +398,8 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
 
   char* ws = static_cast<char*>(workspace);
   float* acc = reinterpret_cast<float*>(ws);
+  CUtensorMap mdq;
+  if (!encode_map_f32_acc(&mdq, acc, static_cast<int>(BH), L, d)) return FA_ERR_LAUNCH;
   float* nlse2 = reinterpret_cast<float*>(ws + w.acc_bytes);
   float* nds = reinterpret_cast<float*>(ws + w.acc_bytes + w.row_bytes);
   const int Lp = static_cast<int>(n_kv * 128);
@@ -422,10 +442,10 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint16_t* dq16 = static_cast<uint16_t*>(dq);
   if (d == 64)
-    return causal ? launch_bwd<64, true>(mq, mk, mv, mdo, args, pre, dq16, s, dev)
-                  : launch_bwd<64, false>(mq, mk, mv, mdo, args, pre, dq16, s, dev);
-  return causal ? launch_bwd<128, true>(mq, mk, mv, mdo, args, pre, dq16, s, dev)
-                : launch_bwd<128, false>(mq, mk, mv, mdo, args, pre, dq16, s, dev);
+    return causal ? launch_bwd<64, true>(mq, mk, mv, mdo, mdq, args, pre, dq16, s, dev)
+                  : launch_bwd<64, false>(mq, mk, mv, mdo, mdq, args, pre, dq16, s, dev);
+  return causal ? launch_bwd<128, true>(mq, mk, mv, mdo, mdq, args, pre, dq16, s, dev)
+                : launch_bwd<128, false>(mq, mk, mv, mdo, mdq, args, pre, dq16, s, dev);
 }
 
 int fa_device_status(fa_stream_t stream, int clear) {

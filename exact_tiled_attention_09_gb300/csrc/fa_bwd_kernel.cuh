@@ -76,6 +76,7 @@ enum : uint32_t {
   SITE_B_DS = 14,
   SITE_B_DQ = 15,
   SITE_B_DQFREE = 16,
+  SITE_B_ALIGN = 17,  // not a wait: the shared-memory base left too little slack
 };
 
 template <int D>
@@ -85,16 +86,26 @@ struct BwdCfg {
   static constexpr int TILE_BYTES = 128 * D * 2;
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = TILE_BYTES;
-  static constexpr int STAGE_OFF = 2 * TILE_BYTES;      // stage s: Q at +0, dO at +TILE
-  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+  // stage s: Q at +0, dO at +TILE, -lse*log2e [128] at +2*TILE, -scale*D
+  // [128] at +2*TILE+512.  After dQ_i is final the Q/dO part (exactly the
+  // size of the fp32 dQ tile) stages dQ_i for the reduce into global memory.
+  static constexpr int STAGE_OFF = 2 * TILE_BYTES;
+  static constexpr int ROWTERM_OFF = 2 * TILE_BYTES;
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES + 1024;
   static constexpr int DS_OFF = STAGE_OFF + BWD_STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = DS_OFF + BWD_DS_BYTES;
   // kv_full, full[S], empty[S], s_full, dp_full, p_ready, ds_ready, dq_full,
   // dq_free, drain
   static constexpr int NBAR = 1 + 2 * BWD_STAGES + 7;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-  static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + alignment slack
-  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  // The tiles need a 1024-byte aligned base; the launch adds as much slack
+  // as the 227 KB budget leaves (up to 1024 bytes) and the kernel checks the
+  // slack it actually needs.
+  static constexpr int USED_BYTES = MISC_OFF + 16;
+  static constexpr int SLACK = (232448 - USED_BYTES) < 1024 ? (232448 - USED_BYTES) / 16 * 16 : 1024;
+  static constexpr int SMEM_BYTES = USED_BYTES + SLACK;
+  static_assert(SLACK >= 0 && SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(BOXES * 4 * 2 * 4096 == 2 * TILE_BYTES, "dQ staging fills the Q/dO part");
   static constexpr uint32_t S_COL = 0;
   static constexpr uint32_t DP_COL = 128;
   static constexpr uint32_t DV_COL = 256;
@@ -198,18 +209,28 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                  const BwdArgs args) {
+                  const __grid_constant__ CUtensorMap tmdQ, const BwdArgs args) {
   using C = BwdCfg<D>;
   constexpr uint32_t BOX = 128 * 64 * 2;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - raw);
+  if (base - raw > static_cast<uint32_t>(C::SLACK)) {
+    // Not enough room to align the tiles: report and leave before any
+    // barrier, copy or tensor-memory allocation (uniform across the CTA).
+    if (threadIdx.x == 0) atomicOr(args.status, 1u << SITE_B_ALIGN);
+    return;
+  }
 
   const uint32_t sK = base + C::K_OFF;
   const uint32_t sV = base + C::V_OFF;
   auto sQ = [&](int st) { return base + C::STAGE_OFF + st * C::STAGE_BYTES; };
   auto sdO = [&](int st) { return base + C::STAGE_OFF + st * C::STAGE_BYTES + C::TILE_BYTES; };
+  // per-query terms of stage st: -lse*log2e at +0, -scale*D at +512 (bytes)
+  auto rowterms = [&](int st) {
+    return base_ptr + C::STAGE_OFF + st * C::STAGE_BYTES + C::ROWTERM_OFF;
+  };
   const uint32_t sDS = base + C::DS_OFF;
   uint8_t* const ds_ptr = base_ptr + C::DS_OFF;
   const uint32_t bars = base + C::BAR_OFF;
@@ -251,7 +272,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     mbar_init(bar_kv, 1);
     for (int s = 0; s < BWD_STAGES; ++s) {
       mbar_init(bar_full(s), 1);
-      mbar_init(bar_empty(s), 1);
+      mbar_init(bar_empty(s), 8);  // each gradient warp, once its dQ reduce has read the stage
     }
     mbar_init(bar_s, 1);
     mbar_init(bar_dp, 1);
@@ -268,6 +289,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmdO);
+    tma_prefetch_desc(&tmdQ);
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -303,12 +325,16 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         break;
       }
       if (elect_one()) {
-        mbar_arrive_expect_tx(bar_full(st), 2 * C::TILE_BYTES);
+        mbar_arrive_expect_tx(bar_full(st), 2 * C::TILE_BYTES + 1024);
         const int row = (q_first + issued) * 128;
         for (int c = 0; c < C::BOXES; ++c) {
           tma_load_3d(sQ(st) + c * BOX, &tmQ, bar_full(st), c * 64, row, bh);
           tma_load_3d(sdO(st) + c * BOX, &tmdO, bar_full(st), c * 64, row, bh);
         }
+        const size_t term = static_cast<size_t>(bh) * args.Lp + row;
+        const uint32_t terms = smem_u32(rowterms(st));
+        bulk_load_1d(terms, args.nlse2 + term, 512, bar_full(st));
+        bulk_load_1d(terms + 512, args.nds + term, 512, bar_full(st));
       }
       __syncwarp();
     }
@@ -378,7 +404,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           mma_ss(tmem + C::DP_COL, sdesc_sw128(sDS + kk * 2048, BOX, 1024),
                  sdesc_sw128(sK + kk * 2048, BOX, 1024), ID_DQ, kk > 0 ? 1u : 0u);
         mma_commit(bar_dq);
-        mma_commit(bar_empty(st));
       }
       __syncwarp();
       if (i + 1 < n_i) {
@@ -409,14 +434,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const bool key_ok = key < L;
     const uint64_t sl2x2 = f2_pack(args.scale_log2, args.scale_log2);
     const uint64_t scale2 = f2_pack(args.scale, args.scale);
-    const float* const nlse_head = args.nlse2 + static_cast<size_t>(bh) * args.Lp;
-    const float* const nds_head = args.nds + static_cast<size_t>(bh) * args.Lp;
     bool ok = true;
 
     for (int i = 0; i < n_i; ++i) {
       const int qb = q_first + i;
-      const int qh0 = qb * 128 + 64 * h;  // first query of this warp's half
+      const int st = i % BWD_STAGES;
       const bool diag = CAUSAL && qb == jblk;
+      const float* const terms = reinterpret_cast<const float*>(rowterms(st)) + 64 * h;
 
       // P^T = exp2(S^T * scale*log2e - lse*log2e), kept in fp32 for dS and
       // written to TMEM as bf16 (the A operand of dV += P^T dO).
@@ -432,7 +456,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         tmem_ld32(lane_base + C::S_COL + 64 * h + 32 * c, sr);
         tmem_wait_ld();
         reg_fence32(sr);
-        const float4* nl = reinterpret_cast<const float4*>(nlse_head + qh0 + 32 * c);
+        const float4* nl = reinterpret_cast<const float4*>(terms + 32 * c);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
@@ -460,7 +484,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p);
+      if (lane == 0) {
+        mbar_arrive(bar_p);
+        // The previous block's dQ reduce read its stage from shared memory;
+        // once that read is done the producer may refill the stage.
+        if (i > 0) {
+          bulk_wait_group_read0();
+          mbar_arrive(bar_empty((i - 1) % BWD_STAGES));
+        }
+      }
 
       // dS^T = P^T (.) (scale * dP^T - scale * D), bf16 into the 128B-swizzled
       // dS tile: row = key, box h holds this half's 64 queries.
@@ -475,7 +507,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         tmem_ld32(lane_base + C::DP_COL + 64 * h + 32 * c, dr);
         tmem_wait_ld();
         reg_fence32(dr);
-        const float4* nd = reinterpret_cast<const float4*>(nds_head + qh0 + 32 * c);
+        const float4* nd = reinterpret_cast<const float4*>(terms + 128 + 32 * c);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
@@ -505,8 +537,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ds);
 
-      // dQ_i: copy this warp's D/2 columns out of TMEM, release the columns,
-      // then add them into the fp32 accumulator (row = query qb*128 + r).
+      // dQ_i: copy this warp's D/2 columns out of TMEM and release them, then
+      // stage them in the block's Q/dO buffers (every MMA that read Q_i and
+      // dO_i is complete: the dq_full arrival follows them) and add them into
+      // the fp32 accumulator with a TMA reduce.  Staging: D/64 boxes of
+      // 32 rows x 32 floats per warp, 128-byte swizzled (16-byte chunk u of
+      // row r at chunk u ^ (r % 8)); rows past L are skipped by the reduce.
       if (!__all_sync(0xffffffffu, mbar_wait(bar_dq, i & 1, ctl, SITE_B_DQ))) {
         ok = false;
         break;
@@ -521,19 +557,31 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dqfree);
-      const int qrow = qb * 128 + r;
-      if (qrow < L) {
-        float4* dst = reinterpret_cast<float4*>(
-            args.dq_acc + (static_cast<size_t>(bh) * L + qrow) * D + (D / 2) * h);
+      const uint32_t stage_base = sQ(st);
+      uint8_t* const stage_ptr = base_ptr + C::STAGE_OFF + st * C::STAGE_BYTES;
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
+      for (int c = 0; c < D / 64; ++c) {
+        const int box = (quarter * 2 + h) * (D / 64) + c;
+        uint8_t* const row_ptr = stage_ptr + box * 4096 + lane * 128;
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            atomicAdd(dst + 8 * c + (e >> 2),
-                      make_float4(__uint_as_float(qv[c][e]), __uint_as_float(qv[c][e + 1]),
-                                  __uint_as_float(qv[c][e + 2]), __uint_as_float(qv[c][e + 3])));
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(row_ptr + ((u ^ (lane & 7)) * 16)) =
+              make_uint4(qv[c][4 * u], qv[c][4 * u + 1], qv[c][4 * u + 2], qv[c][4 * u + 3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          const int box = (quarter * 2 + h) * (D / 64) + c;
+          tma_reduce_add_3d(&tmdQ, stage_base + box * 4096, (D / 2) * h + 32 * c,
+                            qb * 128 + quarter * 32, bh);
+        }
+        bulk_commit_group();
       }
     }
+    // The CTA's shared memory must outlive the last reduce.
+    if (lane == 0) bulk_wait_group0();
 
     // Epilogue: the last dq_full arrival came after every MMA of the CTA, so
     // dV_j and dK_j are final.  bf16 (round to nearest even), rows < L.
