@@ -34,7 +34,7 @@
 //   warp 0      MMA issuer, owner of the tensor memory (whole warp polls,
 //               one elected lane issues)
 //   warp 1      TMA producer: K_j, V_j once; Q_i and dO_i into a two-stage
-//               ring (full/empty mbarriers)
+//               ring (full mbarriers); issues the dQ reduce-adds
 //   warps 2..9  gradient warps: warp w handles TMEM lanes 32*(w%4)..+31
 //               (its keys) and query columns 64*h..64*h+63, h = (w-2)/4
 //
@@ -49,12 +49,18 @@
 // publishes S_{i+1} also proves dK_i and dQ_i have read the dS tile, so the
 // gradient warps may overwrite it; dP_{i+1} waits until the gradient warps
 // have copied dQ_i out of its columns.
+//
+// dQ_i leaves through the producer warp: the gradient warps stage it in the
+// block's Q/dO buffers (free once dQ_i is final) and arrive on dq_staged;
+// the producer issues the tensor reduce-adds, waits until they have read the
+// stage, and only then loads block i+2 into it.
 #pragma once
 
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "sm103_ptx.cuh"
 
@@ -69,7 +75,7 @@ constexpr int BWD_DS_BYTES = 128 * 128 * 2;  // dS^T tile, two 128 x 64 boxes
 enum : uint32_t {
   SITE_B_KV = 8,
   SITE_B_FULL = 9,
-  SITE_B_EMPTY = 10,
+  SITE_B_DQST = 10,
   SITE_B_S = 11,
   SITE_B_DP = 12,
   SITE_B_P = 13,
@@ -94,8 +100,8 @@ struct BwdCfg {
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES + 1024;
   static constexpr int DS_OFF = STAGE_OFF + BWD_STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = DS_OFF + BWD_DS_BYTES;
-  // kv_full, full[S], empty[S], s_full, dp_full, p_ready, ds_ready, dq_full,
-  // dq_free, drain
+  // kv_full, full[S], dq_staged[S], s_full, dp_full, p_ready, ds_ready,
+  // dq_full, dq_free, drain
   static constexpr int NBAR = 1 + 2 * BWD_STAGES + 7;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   // The tiles need a 1024-byte aligned base; the launch adds as much slack
@@ -144,6 +150,37 @@ struct BwdPreArgs {
   long long rows;          // BH * Lp
   float scale;
 };
+
+// 2^x for a pair of floats on the FMA pipe instead of the MUFU unit, which
+// the recomputation of P otherwise saturates (one ex2 per score, 16 per
+// clock per SM).  Range reduction to the nearest integer: t = x + 1.5*2^23
+// rounds x to an integer n held in t's low mantissa bits, f = x - n lies in
+// [-1/2, 1/2], and 2^x = 2^f * 2^n is p(f) with n added to its exponent
+// field ((bits(t) << 23) mod 2^32 == n << 23).  p is the cubic minimax fit
+// of 2^f in relative error on [-1/2, 1/2] (Remez exchange; coefficients
+// from exp2_poly_fit.py, which prints them), max relative error 7.5e-5 in
+// fp32 -- far below the 2^-9 of the bf16 rounding that P undergoes.  x is
+// clamped to -126 first, so -inf and deep underflow give tiny positive
+// values, never NaN.
+constexpr float EXP2_C0 = 0.9999280571937561f;
+constexpr float EXP2_C1 = 0.6932609677314758f;
+constexpr float EXP2_C2 = 0.2426111251115799f;
+constexpr float EXP2_C3 = 0.0551716685295105f;
+
+__device__ __forceinline__ void exp2_fma_pair(float x0, float x1, float& y0, float& y1) {
+  const uint64_t x = f2_pack(fmaxf(x0, -126.f), fmaxf(x1, -126.f));
+  const uint64_t t = f2_add(x, f2_pack(12582912.f, 12582912.f));
+  const uint64_t n = f2_add(t, f2_pack(-12582912.f, -12582912.f));
+  const uint64_t f = f2_fma(n, f2_pack(-1.f, -1.f), x);
+  uint64_t q = f2_fma(f, f2_pack(EXP2_C3, EXP2_C3), f2_pack(EXP2_C2, EXP2_C2));
+  q = f2_fma(q, f, f2_pack(EXP2_C1, EXP2_C1));
+  q = f2_fma(q, f, f2_pack(EXP2_C0, EXP2_C0));
+  float q0, q1, t0, t1;
+  f2_unpack(q, q0, q1);
+  f2_unpack(t, t0, t1);
+  y0 = __uint_as_float(__float_as_uint(q0) + (__float_as_uint(t0) << 23));
+  y1 = __uint_as_float(__float_as_uint(q1) + (__float_as_uint(t1) << 23));
+}
 
 constexpr int BWD_AUX_WARPS = 8;  // rows per block of the pre-pass
 
@@ -236,7 +273,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   const uint32_t bars = base + C::BAR_OFF;
   const uint32_t bar_kv = bars;
   auto bar_full = [&](int s) { return bars + 8u * (1 + s); };
-  auto bar_empty = [&](int s) { return bars + 8u * (1 + BWD_STAGES + s); };
+  // dq_staged of stage s completes once per use of the stage, so it can
+  // never run a phase ahead of the producer: staging block k+2 needs block
+  // k+2 loaded, which the producer does only after consuming block k's phase.
+  auto bar_dqst = [&](int s) { return bars + 8u * (1 + BWD_STAGES + s); };
   const uint32_t bar_s = bars + 8u * (1 + 2 * BWD_STAGES);
   const uint32_t bar_dp = bar_s + 8;
   const uint32_t bar_p = bar_s + 16;
@@ -272,7 +312,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     mbar_init(bar_kv, 1);
     for (int s = 0; s < BWD_STAGES; ++s) {
       mbar_init(bar_full(s), 1);
-      mbar_init(bar_empty(s), 8);  // each gradient warp, once its dQ reduce has read the stage
+      mbar_init(bar_dqst(s), 8);  // one arrival per gradient warp: dQ staged
     }
     mbar_init(bar_s, 1);
     mbar_init(bar_dp, 1);
@@ -315,14 +355,40 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
     }
     __syncwarp();
-    int issued = 0;
+    // dQ of block blk is staged in its stage: add it into the accumulator
+    // (16 or 8 boxes of 32 rows x 32 floats, one per gradient warp and
+    // column group) and wait until the reduces have read the stage.
+    auto reduce_block = [&](int blk) -> bool {
+      if (!warp_wait(bar_dqst(blk % BWD_STAGES),
+                     static_cast<uint32_t>(blk / BWD_STAGES) & 1u, SITE_B_DQST))
+        return false;
+      if (elect_one()) {
+        const int qb = q_first + blk;
+        const uint32_t sb = sQ(blk % BWD_STAGES);
+        for (int quarter = 0; quarter < 4; ++quarter)
+          for (int hh = 0; hh < 2; ++hh)
+            for (int c = 0; c < D / 64; ++c) {
+              const int box = (quarter * 2 + hh) * (D / 64) + c;
+              tma_reduce_add_3d(&tmdQ, sb + box * 4096, (D / 2) * hh + 32 * c,
+                                qb * 128 + quarter * 32, bh);
+            }
+        bulk_commit_group();
+        bulk_wait_group_read0();
+      }
+      __syncwarp();
+      return true;
+    };
+    int issued = 0, reduced = 0;
     bool ok = true;
     for (; issued < n_i; ++issued) {
       const int st = issued % BWD_STAGES;
-      const uint32_t use = static_cast<uint32_t>(issued / BWD_STAGES);
-      if (!warp_wait(bar_empty(st), (use & 1u) ^ 1u, SITE_B_EMPTY)) {
-        ok = false;
-        break;
+      if (issued >= BWD_STAGES) {
+        // the stage still holds block issued-2's dQ: send it out first
+        if (!reduce_block(reduced)) {
+          ok = false;
+          break;
+        }
+        ++reduced;
       }
       if (elect_one()) {
         mbar_arrive_expect_tx(bar_full(st), 2 * C::TILE_BYTES + 1024);
@@ -338,14 +404,20 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
       __syncwarp();
     }
-    if (!ok && lane == 0) {
-      // Let every copy already issued land before the CTA exits.
-      if (!args.test_withhold_kv) mbar_wait_drain(bar_kv, 0, args.timeout_ns);
-      for (int s = 0; s < BWD_STAGES; ++s) {
-        const int n = issued > s ? (issued - 1 - s) / BWD_STAGES + 1 : 0;
-        if (n > 0) mbar_wait_drain(bar_full(s), (n - 1) & 1, args.timeout_ns);
+    for (; ok && reduced < n_i; ++reduced) ok = reduce_block(reduced);
+    if (elect_one()) {
+      if (!ok) {
+        // Let every copy already issued land before the CTA exits.
+        if (!args.test_withhold_kv) mbar_wait_drain(bar_kv, 0, args.timeout_ns);
+        for (int s = 0; s < BWD_STAGES; ++s) {
+          const int n = issued > s ? (issued - 1 - s) / BWD_STAGES + 1 : 0;
+          if (n > 0) mbar_wait_drain(bar_full(s), (n - 1) & 1, args.timeout_ns);
+        }
       }
+      // The CTA's shared memory must outlive the reduces.
+      bulk_wait_group0();
     }
+    __syncwarp();
   } else if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t ID_S = idesc_bf16_f32_ab(128, 128, false, false);
@@ -432,6 +504,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const int key = jblk * 128 + r;
     const bool key_ok = key < L;
+    const bool tail_blk = (jblk + 1) * 128 > L;  // some key of this block is past L
     const uint64_t sl2x2 = f2_pack(args.scale_log2, args.scale_log2);
     const uint64_t scale2 = f2_pack(args.scale, args.scale);
     bool ok = true;
@@ -450,6 +523,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
       tc_fence_after();
       float p[64];
+      // The masks apply only on the causal diagonal block and in the last
+      // key block of a ragged L (both uniform across the CTA); elsewhere
+      // the per-element selects are compiled out.
+      auto phase_a = [&](auto mask_tag) {
+        constexpr bool MASK = decltype(mask_tag)::value;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t sr[32];
@@ -468,12 +546,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), sl2x2,
                            f2_pack(a.z, a.w)),
                     x2, x3);
-          float pe[4] = {ex2_approx(x0), ex2_approx(x1), ex2_approx(x2), ex2_approx(x3)};
+          // half of the exponentials on the MUFU unit, half on the FMA pipe
+          float pe[4] = {ex2_approx(x0), ex2_approx(x1), 0.f, 0.f};
+          exp2_fma_pair(x2, x3, pe[2], pe[3]);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             // causal: key r > query (64h + 32c + e + u) of the same block;
             // keys past L (zero rows of K) never contribute.
-            if ((diag && r > 64 * h + 32 * c + e + u) || !key_ok) pe[u] = 0.f;
+            if constexpr (MASK)
+              if ((diag && r > 64 * h + 32 * c + e + u) || !key_ok) pe[u] = 0.f;
             p[32 * c + e + u] = pe[u];
           }
           pk[e >> 1] = pack_bf16x2(pe[0], pe[1]);
@@ -481,18 +562,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         }
         tmem_st16(lane_base + C::S_COL + 64 * h + 16 * c, pk);
       }
+      };
+      if (diag || tail_blk)
+        phase_a(std::true_type{});
+      else
+        phase_a(std::false_type{});
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar_p);
-        // The previous block's dQ reduce read its stage from shared memory;
-        // once that read is done the producer may refill the stage.
-        if (i > 0) {
-          bulk_wait_group_read0();
-          mbar_arrive(bar_empty((i - 1) % BWD_STAGES));
-        }
-      }
+      if (lane == 0) mbar_arrive(bar_p);
 
       // dS^T = P^T (.) (scale * dP^T - scale * D), bf16 into the 128B-swizzled
       // dS tile: row = key, box h holds this half's 64 queries.
@@ -539,8 +617,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 
       // dQ_i: copy this warp's D/2 columns out of TMEM and release them, then
       // stage them in the block's Q/dO buffers (every MMA that read Q_i and
-      // dO_i is complete: the dq_full arrival follows them) and add them into
-      // the fp32 accumulator with a TMA reduce.  Staging: D/64 boxes of
+      // dO_i is complete: the dq_full arrival follows them) for the
+      // producer's reduce into the fp32 accumulator.  Staging: D/64 boxes of
       // 32 rows x 32 floats per warp, 128-byte swizzled (16-byte chunk u of
       // row r at chunk u ^ (r % 8)); rows past L are skipped by the reduce.
       if (!__all_sync(0xffffffffu, mbar_wait(bar_dq, i & 1, ctl, SITE_B_DQ))) {
@@ -557,7 +635,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dqfree);
-      const uint32_t stage_base = sQ(st);
       uint8_t* const stage_ptr = base_ptr + C::STAGE_OFF + st * C::STAGE_BYTES;
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
@@ -568,20 +645,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           *reinterpret_cast<uint4*>(row_ptr + ((u ^ (lane & 7)) * 16)) =
               make_uint4(qv[c][4 * u], qv[c][4 * u + 1], qv[c][4 * u + 2], qv[c][4 * u + 3]);
       }
-      fence_proxy_async_smem();
+      fence_proxy_async_smem();  // the producer's reduce reads the stage via the async proxy
       __syncwarp();
-      if (lane == 0) {
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          const int box = (quarter * 2 + h) * (D / 64) + c;
-          tma_reduce_add_3d(&tmdQ, stage_base + box * 4096, (D / 2) * h + 32 * c,
-                            qb * 128 + quarter * 32, bh);
-        }
-        bulk_commit_group();
-      }
+      if (lane == 0) mbar_arrive(bar_dqst(st));
     }
-    // The CTA's shared memory must outlive the last reduce.
-    if (lane == 0) bulk_wait_group0();
 
     // Epilogue: the last dq_full arrival came after every MMA of the CTA, so
     // dV_j and dK_j are final.  bf16 (round to nearest even), rows < L.
