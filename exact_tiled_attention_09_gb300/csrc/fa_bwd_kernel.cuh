@@ -45,15 +45,16 @@
 // Order of the MMAs per query block (tcgen05 operations of one thread
 // complete in issue order, which the hand-offs rely on):
 //   dP_i | wait P ready: dV_i | wait dS ready: dK_i, dQ_i | S_{i+1}
-// S_{i+1} overwrites P^T_i only after dV_i has read it; the commit that
-// publishes S_{i+1} also proves dK_i and dQ_i have read the dS tile, so the
-// gradient warps may overwrite it; dP_{i+1} waits until the gradient warps
-// have copied dQ_i out of its columns.
+// S_{i+1} overwrites P^T_i only after dV_i has read it; dP_{i+1} waits until
+// the gradient warps have copied dQ_i out of its columns.
 //
-// dQ_i leaves through the producer warp: the gradient warps stage it in the
-// block's Q/dO buffers (free once dQ_i is final) and arrive on dq_staged;
-// the producer issues the tensor reduce-adds, waits until they have read the
-// stage, and only then loads block i+2 into it.
+// Copies and the dQ path.  Q_i (with its per-query terms) and dO_i have
+// separate full barriers.  dQ_i leaves through the producer warp: the
+// gradient warps stage it in block i's Q and dO buffers (free once dQ_i is
+// final: every MMA that read them is complete) and arrive on dq_staged; the
+// producer issues the tensor reduce-adds as two groups, the boxes in the Q
+// buffer first, and refills the Q buffer (Q_{i+2}, needed first) as soon as
+// that group has been read, the dO buffer after the second.
 #pragma once
 
 #include <cuda.h>
@@ -76,6 +77,7 @@ enum : uint32_t {
   SITE_B_KV = 8,
   SITE_B_FULL = 9,
   SITE_B_DQST = 10,
+
   SITE_B_S = 11,
   SITE_B_DP = 12,
   SITE_B_P = 13,
@@ -93,16 +95,15 @@ struct BwdCfg {
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = TILE_BYTES;
   // stage s: Q at +0, dO at +TILE, -lse*log2e [128] at +2*TILE, -scale*D
-  // [128] at +2*TILE+512.  After dQ_i is final the Q/dO part (exactly the
-  // size of the fp32 dQ tile) stages dQ_i for the reduce into global memory.
+  // [128] at +2*TILE+512.
   static constexpr int STAGE_OFF = 2 * TILE_BYTES;
   static constexpr int ROWTERM_OFF = 2 * TILE_BYTES;
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES + 1024;
   static constexpr int DS_OFF = STAGE_OFF + BWD_STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = DS_OFF + BWD_DS_BYTES;
-  // kv_full, full[S], dq_staged[S], s_full, dp_full, p_ready, ds_ready,
-  // dq_full, dq_free, drain
-  static constexpr int NBAR = 1 + 2 * BWD_STAGES + 7;
+  // kv_full, fullQ[S], fulldO[S], dq_staged[S], s_full, dp_full, p_ready,
+  // ds_ready, dq_full, dq_free, drain
+  static constexpr int NBAR = 1 + 3 * BWD_STAGES + 7;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   // The tiles need a 1024-byte aligned base; the launch adds as much slack
   // as the 227 KB budget leaves (up to 1024 bytes) and the kernel checks the
@@ -111,7 +112,10 @@ struct BwdCfg {
   static constexpr int SLACK = (232448 - USED_BYTES) < 1024 ? (232448 - USED_BYTES) / 16 * 16 : 1024;
   static constexpr int SMEM_BYTES = USED_BYTES + SLACK;
   static_assert(SLACK >= 0 && SMEM_BYTES <= 232448, "shared memory budget");
-  static_assert(BOXES * 4 * 2 * 4096 == 2 * TILE_BYTES, "dQ staging fills the Q/dO part");
+  // dQ staging: 8 * D/64 boxes of 4 KB fill the Q and dO buffers exactly,
+  // the first half in the Q buffer
+  static constexpr int DQ_BOXES = 8 * BOXES;
+  static_assert(DQ_BOXES * 4096 == 2 * TILE_BYTES, "dQ staging fills the Q/dO buffers");
   static constexpr uint32_t S_COL = 0;
   static constexpr uint32_t DP_COL = 128;
   static constexpr uint32_t DV_COL = 256;
@@ -270,14 +274,21 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   };
   const uint32_t sDS = base + C::DS_OFF;
   uint8_t* const ds_ptr = base_ptr + C::DS_OFF;
+  // dQ staging box c of gradient warp (quarter, h), 32 rows x 32 floats:
+  // box b = (quarter*2 + h)*(D/64) + c at 4 KB steps from the Q buffer on.
+  auto dq_box_index = [](int quarter, int h, int c) { return (quarter * 2 + h) * (D / 64) + c; };
+  auto dq_box = [&](int st, int quarter, int h, int c) -> uint32_t {
+    return sQ(st) + dq_box_index(quarter, h, c) * 4096;
+  };
   const uint32_t bars = base + C::BAR_OFF;
   const uint32_t bar_kv = bars;
-  auto bar_full = [&](int s) { return bars + 8u * (1 + s); };
+  auto bar_fullq = [&](int s) { return bars + 8u * (1 + s); };
+  auto bar_fulldo = [&](int s) { return bars + 8u * (1 + BWD_STAGES + s); };
   // dq_staged of stage s completes once per use of the stage, so it can
   // never run a phase ahead of the producer: staging block k+2 needs block
   // k+2 loaded, which the producer does only after consuming block k's phase.
-  auto bar_dqst = [&](int s) { return bars + 8u * (1 + BWD_STAGES + s); };
-  const uint32_t bar_s = bars + 8u * (1 + 2 * BWD_STAGES);
+  auto bar_dqst = [&](int s) { return bars + 8u * (1 + 2 * BWD_STAGES + s); };
+  const uint32_t bar_s = bars + 8u * (1 + 3 * BWD_STAGES);
   const uint32_t bar_dp = bar_s + 8;
   const uint32_t bar_p = bar_s + 16;
   const uint32_t bar_ds = bar_s + 24;
@@ -311,7 +322,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar_kv, 1);
     for (int s = 0; s < BWD_STAGES; ++s) {
-      mbar_init(bar_full(s), 1);
+      mbar_init(bar_fullq(s), 1);
+      mbar_init(bar_fulldo(s), 1);
       mbar_init(bar_dqst(s), 8);  // one arrival per gradient warp: dQ staged
     }
     mbar_init(bar_s, 1);
@@ -344,6 +356,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const bool w = mbar_wait(bar, parity, ctl, site);
     return __all_sync(0xffffffffu, w);
   };
+  auto use_parity = [](int blk) { return static_cast<uint32_t>(blk / BWD_STAGES) & 1u; };
 
   if (warp == 1) {
     // ------------------------------------------------------------ producer
@@ -355,54 +368,72 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
     }
     __syncwarp();
-    // dQ of block blk is staged in its stage: add it into the accumulator
-    // (16 or 8 boxes of 32 rows x 32 floats, one per gradient warp and
-    // column group) and wait until the reduces have read the stage.
+    auto load_q = [&](int blk) {
+      const int st = blk % BWD_STAGES;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(bar_fullq(st), C::TILE_BYTES + 1024);
+        const int row = (q_first + blk) * 128;
+        for (int c = 0; c < C::BOXES; ++c)
+          tma_load_3d(sQ(st) + c * BOX, &tmQ, bar_fullq(st), c * 64, row, bh);
+        const size_t term = static_cast<size_t>(bh) * args.Lp + row;
+        const uint32_t terms = smem_u32(rowterms(st));
+        bulk_load_1d(terms, args.nlse2 + term, 512, bar_fullq(st));
+        bulk_load_1d(terms + 512, args.nds + term, 512, bar_fullq(st));
+      }
+      __syncwarp();
+    };
+    auto load_do = [&](int blk) {
+      const int st = blk % BWD_STAGES;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(bar_fulldo(st), C::TILE_BYTES);
+        const int row = (q_first + blk) * 128;
+        for (int c = 0; c < C::BOXES; ++c)
+          tma_load_3d(sdO(st) + c * BOX, &tmdO, bar_fulldo(st), c * 64, row, bh);
+      }
+      __syncwarp();
+    };
+    // dQ of block blk is staged: add it into the accumulator (one reduce per
+    // box, 32 rows x 32 floats each) in two groups, the boxes in the Q
+    // buffer first.  Returns once the Q buffer has been read; the caller
+    // waits for the rest (bulk_wait_group_read0) before reusing the dO
+    // buffer.
     auto reduce_block = [&](int blk) -> bool {
-      if (!warp_wait(bar_dqst(blk % BWD_STAGES),
-                     static_cast<uint32_t>(blk / BWD_STAGES) & 1u, SITE_B_DQST))
-        return false;
+      const int st = blk % BWD_STAGES;
+      if (!warp_wait(bar_dqst(st), use_parity(blk), SITE_B_DQST)) return false;
       if (elect_one()) {
         const int qb = q_first + blk;
-        const uint32_t sb = sQ(blk % BWD_STAGES);
-        for (int quarter = 0; quarter < 4; ++quarter)
-          for (int hh = 0; hh < 2; ++hh)
-            for (int c = 0; c < D / 64; ++c) {
-              const int box = (quarter * 2 + hh) * (D / 64) + c;
-              tma_reduce_add_3d(&tmdQ, sb + box * 4096, (D / 2) * hh + 32 * c,
-                                qb * 128 + quarter * 32, bh);
-            }
-        bulk_commit_group();
-        bulk_wait_group_read0();
+        for (int half = 0; half < 2; ++half) {
+          for (int quarter = 0; quarter < 4; ++quarter)
+            for (int hh = 0; hh < 2; ++hh)
+              for (int c = 0; c < D / 64; ++c)
+                if ((dq_box_index(quarter, hh, c) >= C::DQ_BOXES / 2) == (half == 1))
+                  tma_reduce_add_3d(&tmdQ, dq_box(st, quarter, hh, c), (D / 2) * hh + 32 * c,
+                                    qb * 128 + quarter * 32, bh);
+          bulk_commit_group();
+        }
+        bulk_wait_group_read1();
       }
       __syncwarp();
       return true;
     };
-    int issued = 0, reduced = 0;
+    // Block k reuses the stage of block k-2: Q_k once the first reduce group
+    // of block k-2 has been read, dO_k once the second has.
+    int q_loads = 0, do_loads = 0, reduced = 0;
     bool ok = true;
-    for (; issued < n_i; ++issued) {
-      const int st = issued % BWD_STAGES;
-      if (issued >= BWD_STAGES) {
-        // the stage still holds block issued-2's dQ: send it out first
-        if (!reduce_block(reduced)) {
-          ok = false;
-          break;
-        }
+    for (int k = 0; k < n_i && ok; ++k) {
+      if (k >= BWD_STAGES) {
+        ok = reduce_block(reduced);
+        if (!ok) break;
         ++reduced;
       }
-      if (elect_one()) {
-        mbar_arrive_expect_tx(bar_full(st), 2 * C::TILE_BYTES + 1024);
-        const int row = (q_first + issued) * 128;
-        for (int c = 0; c < C::BOXES; ++c) {
-          tma_load_3d(sQ(st) + c * BOX, &tmQ, bar_full(st), c * 64, row, bh);
-          tma_load_3d(sdO(st) + c * BOX, &tmdO, bar_full(st), c * 64, row, bh);
-        }
-        const size_t term = static_cast<size_t>(bh) * args.Lp + row;
-        const uint32_t terms = smem_u32(rowterms(st));
-        bulk_load_1d(terms, args.nlse2 + term, 512, bar_full(st));
-        bulk_load_1d(terms + 512, args.nds + term, 512, bar_full(st));
+      load_q(k);
+      ++q_loads;
+      if (k >= BWD_STAGES) {
+        if (elect_one()) bulk_wait_group_read0();
+        __syncwarp();
       }
-      __syncwarp();
+      load_do(k);
+      ++do_loads;
     }
     for (; ok && reduced < n_i; ++reduced) ok = reduce_block(reduced);
     if (elect_one()) {
@@ -410,8 +441,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         // Let every copy already issued land before the CTA exits.
         if (!args.test_withhold_kv) mbar_wait_drain(bar_kv, 0, args.timeout_ns);
         for (int s = 0; s < BWD_STAGES; ++s) {
-          const int n = issued > s ? (issued - 1 - s) / BWD_STAGES + 1 : 0;
-          if (n > 0) mbar_wait_drain(bar_full(s), (n - 1) & 1, args.timeout_ns);
+          const int nq = q_loads > s ? (q_loads - 1 - s) / BWD_STAGES + 1 : 0;
+          const int nd = do_loads > s ? (do_loads - 1 - s) / BWD_STAGES + 1 : 0;
+          if (nq > 0) mbar_wait_drain(bar_fullq(s), (nq - 1) & 1, args.timeout_ns);
+          if (nd > 0) mbar_wait_drain(bar_fulldo(s), (nd - 1) & 1, args.timeout_ns);
         }
       }
       // The CTA's shared memory must outlive the reduces.
@@ -438,7 +471,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       __syncwarp();
     };
     bool ok = warp_wait(bar_kv, 0, SITE_B_KV);
-    if (ok) ok = warp_wait(bar_full(0), 0, SITE_B_FULL);
+    if (ok) ok = warp_wait(bar_fullq(0), 0, SITE_B_FULL);
     if (ok) {
       tc_fence_after();
       issue_kmajor(C::S_COL, sK, sQ(0), bar_s);
@@ -448,8 +481,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       if (i > 0) {
         ok = warp_wait(bar_dqfree, (i - 1) & 1, SITE_B_DQFREE);
         if (!ok) break;
-        tc_fence_after();
       }
+      ok = warp_wait(bar_fulldo(st), use_parity(i), SITE_B_FULL);
+      if (!ok) break;
+      tc_fence_after();
       issue_kmajor(C::DP_COL, sV, sdO(st), bar_dp);
       // dV += P^T dO_i once the gradient warps have written P^T.
       ok = warp_wait(bar_p, i & 1, SITE_B_P);
@@ -480,8 +515,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       __syncwarp();
       if (i + 1 < n_i) {
         const int st2 = (i + 1) % BWD_STAGES;
-        ok = warp_wait(bar_full(st2), static_cast<uint32_t>((i + 1) / BWD_STAGES) & 1u,
-                       SITE_B_FULL);
+        ok = warp_wait(bar_fullq(st2), use_parity(i + 1), SITE_B_FULL);
         if (!ok) break;
         tc_fence_after();
         issue_kmajor(C::S_COL, sK, sQ(st2), bar_s);
@@ -616,11 +650,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       if (lane == 0) mbar_arrive(bar_ds);
 
       // dQ_i: copy this warp's D/2 columns out of TMEM and release them, then
-      // stage them in the block's Q/dO buffers (every MMA that read Q_i and
-      // dO_i is complete: the dq_full arrival follows them) for the
-      // producer's reduce into the fp32 accumulator.  Staging: D/64 boxes of
-      // 32 rows x 32 floats per warp, 128-byte swizzled (16-byte chunk u of
-      // row r at chunk u ^ (r % 8)); rows past L are skipped by the reduce.
+      // stage them in block i's Q/dO buffers (every MMA that read Q_i and dO_i
+      // is complete: the dq_full arrival follows them) for the producer's
+      // reduce into the fp32 accumulator.  A box is 32 rows x 32 floats,
+      // 128-byte swizzled (16-byte chunk u of row r at chunk u ^ (r % 8));
+      // rows past L are skipped by the reduce.
       if (!__all_sync(0xffffffffu, mbar_wait(bar_dq, i & 1, ctl, SITE_B_DQ))) {
         ok = false;
         break;
@@ -635,11 +669,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dqfree);
-      uint8_t* const stage_ptr = base_ptr + C::STAGE_OFF + st * C::STAGE_BYTES;
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
-        const int box = (quarter * 2 + h) * (D / 64) + c;
-        uint8_t* const row_ptr = stage_ptr + box * 4096 + lane * 128;
+        uint8_t* const row_ptr = base_ptr + (dq_box(st, quarter, h, c) - base) + lane * 128;
 #pragma unroll
         for (int u = 0; u < 8; ++u)
           *reinterpret_cast<uint4*>(row_ptr + ((u ^ (lane & 7)) * 16)) =
