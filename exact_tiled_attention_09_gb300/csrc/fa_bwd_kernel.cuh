@@ -33,8 +33,9 @@
 // Warp roles (320 threads):
 //   warp 0      MMA issuer, owner of the tensor memory (whole warp polls,
 //               one elected lane issues)
-//   warp 1      TMA producer: K_j, V_j once; Q_i and dO_i into a two-stage
-//               ring (full mbarriers); issues the dQ reduce-adds
+//   warp 1      TMA producer: K_j, V_j once; Q_i and dO_i into a ring of
+//               stages (two at d = 128, three at d = 64); issues the dQ
+//               reduce-adds
 //   warps 2..9  gradient warps: warp w handles TMEM lanes 32*(w%4)..+31
 //               (its keys) and query columns 64*h..64*h+63, h = (w-2)/4
 //
@@ -44,9 +45,15 @@
 //
 // Order of the MMAs per query block (tcgen05 operations of one thread
 // complete in issue order, which the hand-offs rely on):
-//   dP_i | wait P ready: dV_i | wait dS ready: dK_i, dQ_i | S_{i+1}
-// S_{i+1} overwrites P^T_i only after dV_i has read it; dP_{i+1} waits until
-// the gradient warps have copied dQ_i out of its columns.
+//   d = 128: dP_i | wait P ready: dV_i | wait dS ready: dK_i, dQ_i | S_{i+1}
+//   d = 64:  dP_i | wait P ready: dV_i, S_{i+1} | wait dS ready: dK_i, dQ_i
+// and the gradient warps work on phases A (P), B (dS), C (dQ out) as
+// A(i) B(i) C(i) at d = 128 and A(0), then B(i) A(i+1) C(i) at d = 64, where
+// the MMA work per block is half as large and P of the next block is
+// computed while dK_i and dQ_i run.  S_{i+1} overwrites P^T_i only after dV_i
+// has read it; dP_{i+1} waits until the gradient warps have copied dQ_i out
+// of its columns, so its commit also proves dK_i and dQ_i have read the dS
+// tile before the gradient warps write dS_{i+1}.
 //
 // Copies and the dQ path.  Q_i (with its per-query terms) and dO_i have
 // separate full barriers.  dQ_i leaves through the producer warp: the
@@ -68,7 +75,6 @@
 namespace fa {
 
 constexpr int BWD_THREADS = 320;
-constexpr int BWD_STAGES = 2;
 constexpr int BWD_FIRST_GRAD_WARP = 2;
 constexpr int BWD_DS_BYTES = 128 * 128 * 2;  // dS^T tile, two 128 x 64 boxes
 
@@ -92,6 +98,13 @@ struct BwdCfg {
   static_assert(D == 64 || D == 128, "head dimension must be 64 or 128");
   static constexpr int BOXES = D / 64;
   static constexpr int TILE_BYTES = 128 * D * 2;
+  // Q/dO stages.  At d = 64 there is room for three, and the pipeline runs
+  // S_{i+1} right behind dV_i so that P of the next block is computed while
+  // dK_i and dQ_i run (EARLY_S); the third stage gives the copy of Q_{i+1}
+  // the time that the dQ reduce of the stage's previous block takes.  At
+  // d = 128 two stages fill shared memory and S_{i+1} follows dQ_i.
+  static constexpr int STAGES = (D == 64) ? 3 : 2;
+  static constexpr bool EARLY_S = (D == 64);
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = TILE_BYTES;
   // stage s: Q at +0, dO at +TILE, -lse*log2e [128] at +2*TILE, -scale*D
@@ -99,11 +112,11 @@ struct BwdCfg {
   static constexpr int STAGE_OFF = 2 * TILE_BYTES;
   static constexpr int ROWTERM_OFF = 2 * TILE_BYTES;
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES + 1024;
-  static constexpr int DS_OFF = STAGE_OFF + BWD_STAGES * STAGE_BYTES;
+  static constexpr int DS_OFF = STAGE_OFF + STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = DS_OFF + BWD_DS_BYTES;
   // kv_full, fullQ[S], fulldO[S], dq_staged[S], s_full, dp_full, p_ready,
   // ds_ready, dq_full, dq_free, drain
-  static constexpr int NBAR = 1 + 3 * BWD_STAGES + 7;
+  static constexpr int NBAR = 1 + 3 * STAGES + 7;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   // The tiles need a 1024-byte aligned base; the launch adds as much slack
   // as the 227 KB budget leaves (up to 1024 bytes) and the kernel checks the
@@ -283,12 +296,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   const uint32_t bars = base + C::BAR_OFF;
   const uint32_t bar_kv = bars;
   auto bar_fullq = [&](int s) { return bars + 8u * (1 + s); };
-  auto bar_fulldo = [&](int s) { return bars + 8u * (1 + BWD_STAGES + s); };
+  auto bar_fulldo = [&](int s) { return bars + 8u * (1 + C::STAGES + s); };
   // dq_staged of stage s completes once per use of the stage, so it can
   // never run a phase ahead of the producer: staging block k+2 needs block
   // k+2 loaded, which the producer does only after consuming block k's phase.
-  auto bar_dqst = [&](int s) { return bars + 8u * (1 + 2 * BWD_STAGES + s); };
-  const uint32_t bar_s = bars + 8u * (1 + 3 * BWD_STAGES);
+  auto bar_dqst = [&](int s) { return bars + 8u * (1 + 2 * C::STAGES + s); };
+  const uint32_t bar_s = bars + 8u * (1 + 3 * C::STAGES);
   const uint32_t bar_dp = bar_s + 8;
   const uint32_t bar_p = bar_s + 16;
   const uint32_t bar_ds = bar_s + 24;
@@ -321,7 +334,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar_kv, 1);
-    for (int s = 0; s < BWD_STAGES; ++s) {
+    for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar_fullq(s), 1);
       mbar_init(bar_fulldo(s), 1);
       mbar_init(bar_dqst(s), 8);  // one arrival per gradient warp: dQ staged
@@ -356,7 +369,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const bool w = mbar_wait(bar, parity, ctl, site);
     return __all_sync(0xffffffffu, w);
   };
-  auto use_parity = [](int blk) { return static_cast<uint32_t>(blk / BWD_STAGES) & 1u; };
+  auto use_parity = [](int blk) { return static_cast<uint32_t>(blk / C::STAGES) & 1u; };
 
   if (warp == 1) {
     // ------------------------------------------------------------ producer
@@ -369,7 +382,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     }
     __syncwarp();
     auto load_q = [&](int blk) {
-      const int st = blk % BWD_STAGES;
+      const int st = blk % C::STAGES;
       if (elect_one()) {
         mbar_arrive_expect_tx(bar_fullq(st), C::TILE_BYTES + 1024);
         const int row = (q_first + blk) * 128;
@@ -383,7 +396,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       __syncwarp();
     };
     auto load_do = [&](int blk) {
-      const int st = blk % BWD_STAGES;
+      const int st = blk % C::STAGES;
       if (elect_one()) {
         mbar_arrive_expect_tx(bar_fulldo(st), C::TILE_BYTES);
         const int row = (q_first + blk) * 128;
@@ -398,7 +411,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     // waits for the rest (bulk_wait_group_read0) before reusing the dO
     // buffer.
     auto reduce_block = [&](int blk) -> bool {
-      const int st = blk % BWD_STAGES;
+      const int st = blk % C::STAGES;
       if (!warp_wait(bar_dqst(st), use_parity(blk), SITE_B_DQST)) return false;
       if (elect_one()) {
         const int qb = q_first + blk;
@@ -421,14 +434,14 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     int q_loads = 0, do_loads = 0, reduced = 0;
     bool ok = true;
     for (int k = 0; k < n_i && ok; ++k) {
-      if (k >= BWD_STAGES) {
+      if (k >= C::STAGES) {
         ok = reduce_block(reduced);
         if (!ok) break;
         ++reduced;
       }
       load_q(k);
       ++q_loads;
-      if (k >= BWD_STAGES) {
+      if (k >= C::STAGES) {
         if (elect_one()) bulk_wait_group_read0();
         __syncwarp();
       }
@@ -440,9 +453,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       if (!ok) {
         // Let every copy already issued land before the CTA exits.
         if (!args.test_withhold_kv) mbar_wait_drain(bar_kv, 0, args.timeout_ns);
-        for (int s = 0; s < BWD_STAGES; ++s) {
-          const int nq = q_loads > s ? (q_loads - 1 - s) / BWD_STAGES + 1 : 0;
-          const int nd = do_loads > s ? (do_loads - 1 - s) / BWD_STAGES + 1 : 0;
+        for (int s = 0; s < C::STAGES; ++s) {
+          const int nq = q_loads > s ? (q_loads - 1 - s) / C::STAGES + 1 : 0;
+          const int nd = do_loads > s ? (do_loads - 1 - s) / C::STAGES + 1 : 0;
           if (nq > 0) mbar_wait_drain(bar_fullq(s), (nq - 1) & 1, args.timeout_ns);
           if (nd > 0) mbar_wait_drain(bar_fulldo(s), (nd - 1) & 1, args.timeout_ns);
         }
@@ -470,6 +483,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
       __syncwarp();
     };
+    auto issue_next_s = [&](int blk) -> bool {
+      const int st2 = blk % C::STAGES;
+      if (!warp_wait(bar_fullq(st2), use_parity(blk), SITE_B_FULL)) return false;
+      tc_fence_after();
+      issue_kmajor(C::S_COL, sK, sQ(st2), bar_s);
+      return true;
+    };
     bool ok = warp_wait(bar_kv, 0, SITE_B_KV);
     if (ok) ok = warp_wait(bar_fullq(0), 0, SITE_B_FULL);
     if (ok) {
@@ -477,7 +497,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       issue_kmajor(C::S_COL, sK, sQ(0), bar_s);
     }
     for (int i = 0; i < n_i && ok; ++i) {
-      const int st = i % BWD_STAGES;
+      const int st = i % C::STAGES;
       if (i > 0) {
         ok = warp_wait(bar_dqfree, (i - 1) & 1, SITE_B_DQFREE);
         if (!ok) break;
@@ -497,6 +517,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                  sdesc_sw128(sdO(st) + kk * 2048, BOX, 1024), ID_DV, (i > 0 || kk > 0) ? 1u : 0u);
       }
       __syncwarp();
+      if (C::EARLY_S && i + 1 < n_i) {
+        ok = issue_next_s(i + 1);  // S_{i+1} behind dV_i, which has read P^T_i
+        if (!ok) break;
+      }
       // dK += dS^T Q_i and dQ_i = dS K_j once dS^T is in shared memory.
       ok = warp_wait(bar_ds, i & 1, SITE_B_DS);
       if (!ok) break;
@@ -513,12 +537,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         mma_commit(bar_dq);
       }
       __syncwarp();
-      if (i + 1 < n_i) {
-        const int st2 = (i + 1) % BWD_STAGES;
-        ok = warp_wait(bar_fullq(st2), use_parity(i + 1), SITE_B_FULL);
+      if (!C::EARLY_S && i + 1 < n_i) {
+        ok = issue_next_s(i + 1);
         if (!ok) break;
-        tc_fence_after();
-        issue_kmajor(C::S_COL, sK, sQ(st2), bar_s);
       }
     }
     if (!ok) {
@@ -541,95 +562,99 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const bool tail_blk = (jblk + 1) * 128 > L;  // some key of this block is past L
     const uint64_t sl2x2 = f2_pack(args.scale_log2, args.scale_log2);
     const uint64_t scale2 = f2_pack(args.scale, args.scale);
-    bool ok = true;
+    auto terms_of = [&](int i) {
+      return reinterpret_cast<const float*>(rowterms(i % C::STAGES)) + 64 * h;
+    };
+    float p[64];  // P^T of this warp's 64 queries, block of the last phase A
 
-    for (int i = 0; i < n_i; ++i) {
-      const int qb = q_first + i;
-      const int st = i % BWD_STAGES;
-      const bool diag = CAUSAL && qb == jblk;
-      const float* const terms = reinterpret_cast<const float*>(rowterms(st)) + 64 * h;
-
-      // P^T = exp2(S^T * scale*log2e - lse*log2e), kept in fp32 for dS and
-      // written to TMEM as bf16 (the A operand of dV += P^T dO).
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_s, i & 1, ctl, SITE_B_S))) {
-        ok = false;
-        break;
-      }
+    // Phase A of block i: P^T = exp2(S^T * scale*log2e - lse*log2e), kept in
+    // fp32 for dS and written to TMEM as bf16 (the A operand of
+    // dV += P^T dO).  The masks apply only on the causal diagonal block and
+    // in the last key block of a ragged L (both uniform across the CTA);
+    // elsewhere the per-element selects are compiled out.
+    auto phase_a = [&](int i) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_s, i & 1, ctl, SITE_B_S))) return false;
       tc_fence_after();
-      float p[64];
-      // The masks apply only on the causal diagonal block and in the last
-      // key block of a ragged L (both uniform across the CTA); elsewhere
-      // the per-element selects are compiled out.
-      auto phase_a = [&](auto mask_tag) {
+      const int qb = q_first + i;
+      const bool diag = CAUSAL && qb == jblk;
+      const float* const terms = terms_of(i);
+      uint32_t sr[2][32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) tmem_ld32(lane_base + C::S_COL + 64 * h + 32 * c, sr[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) reg_fence32(sr[c]);
+      auto compute = [&](auto mask_tag) {
         constexpr bool MASK = decltype(mask_tag)::value;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t sr[32];
-        tmem_ld32(lane_base + C::S_COL + 64 * h + 32 * c, sr);
-        tmem_wait_ld();
-        reg_fence32(sr);
-        const float4* nl = reinterpret_cast<const float4*>(terms + 32 * c);
-        uint32_t pk[16];
+        for (int c = 0; c < 2; ++c) {
+          const float4* nl = reinterpret_cast<const float4*>(terms + 32 * c);
+          uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 a = nl[e >> 2];
-          float x0, x1, x2, x3;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl2x2,
-                           f2_pack(a.x, a.y)),
-                    x0, x1);
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), sl2x2,
-                           f2_pack(a.z, a.w)),
-                    x2, x3);
-          // half of the exponentials on the MUFU unit, half on the FMA pipe
-          float pe[4] = {ex2_approx(x0), ex2_approx(x1), 0.f, 0.f};
-          exp2_fma_pair(x2, x3, pe[2], pe[3]);
+          for (int e = 0; e < 32; e += 4) {
+            const float4 a = nl[e >> 2];
+            float x0, x1, x2, x3;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])),
+                             sl2x2, f2_pack(a.x, a.y)),
+                      x0, x1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][e + 2]), __uint_as_float(sr[c][e + 3])),
+                             sl2x2, f2_pack(a.z, a.w)),
+                      x2, x3);
+            // half of the exponentials on the MUFU unit, half on the FMA pipe
+            float pe[4] = {ex2_approx(x0), ex2_approx(x1), 0.f, 0.f};
+            exp2_fma_pair(x2, x3, pe[2], pe[3]);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            // causal: key r > query (64h + 32c + e + u) of the same block;
-            // keys past L (zero rows of K) never contribute.
-            if constexpr (MASK)
-              if ((diag && r > 64 * h + 32 * c + e + u) || !key_ok) pe[u] = 0.f;
-            p[32 * c + e + u] = pe[u];
+            for (int u = 0; u < 4; ++u) {
+              // causal: key r > query (64h + 32c + e + u) of the same block;
+              // keys past L (zero rows of K) never contribute.
+              if constexpr (MASK)
+                if ((diag && r > 64 * h + 32 * c + e + u) || !key_ok) pe[u] = 0.f;
+              p[32 * c + e + u] = pe[u];
+            }
+            pk[e >> 1] = pack_bf16x2(pe[0], pe[1]);
+            pk[(e >> 1) + 1] = pack_bf16x2(pe[2], pe[3]);
           }
-          pk[e >> 1] = pack_bf16x2(pe[0], pe[1]);
-          pk[(e >> 1) + 1] = pack_bf16x2(pe[2], pe[3]);
+          tmem_st16(lane_base + C::S_COL + 64 * h + 16 * c, pk);
         }
-        tmem_st16(lane_base + C::S_COL + 64 * h + 16 * c, pk);
-      }
       };
       if (diag || tail_blk)
-        phase_a(std::true_type{});
+        compute(std::true_type{});
       else
-        phase_a(std::false_type{});
+        compute(std::false_type{});
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p);
+      return true;
+    };
 
-      // dS^T = P^T (.) (scale * dP^T - scale * D), bf16 into the 128B-swizzled
-      // dS tile: row = key, box h holds this half's 64 queries.
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_dp, i & 1, ctl, SITE_B_DP))) {
-        ok = false;
-        break;
-      }
+    // Phase B of block i: dS^T = P^T (.) (scale * dP^T - scale * D), bf16
+    // into the 128B-swizzled dS tile: row = key, box h holds this half's 64
+    // queries.
+    auto phase_b = [&](int i) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_dp, i & 1, ctl, SITE_B_DP))) return false;
       tc_fence_after();
+      const float* const terms = terms_of(i);
+      uint32_t dr[2][32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) tmem_ld32(lane_base + C::DP_COL + 64 * h + 32 * c, dr[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) reg_fence32(dr[c]);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        uint32_t dr[32];
-        tmem_ld32(lane_base + C::DP_COL + 64 * h + 32 * c, dr);
-        tmem_wait_ld();
-        reg_fence32(dr);
         const float4* nd = reinterpret_cast<const float4*>(terms + 128 + 32 * c);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           const float4 b = nd[e >> 2];
           float d0, d1, d2, d3;
-          f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
+          f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(dr[c][e]), __uint_as_float(dr[c][e + 1])),
                                   scale2, f2_pack(b.x, b.y)),
                            f2_pack(p[32 * c + e], p[32 * c + e + 1])),
                     d0, d1);
-          f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(dr[e + 2]), __uint_as_float(dr[e + 3])),
+          f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(dr[c][e + 2]),
+                                          __uint_as_float(dr[c][e + 3])),
                                   scale2, f2_pack(b.z, b.w)),
                            f2_pack(p[32 * c + e + 2], p[32 * c + e + 3])),
                     d2, d3);
@@ -648,18 +673,19 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ds);
+      return true;
+    };
 
-      // dQ_i: copy this warp's D/2 columns out of TMEM and release them, then
-      // stage them in block i's Q/dO buffers (every MMA that read Q_i and dO_i
-      // is complete: the dq_full arrival follows them) for the producer's
-      // reduce into the fp32 accumulator.  A box is 32 rows x 32 floats,
-      // 128-byte swizzled (16-byte chunk u of row r at chunk u ^ (r % 8));
-      // rows past L are skipped by the reduce.
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_dq, i & 1, ctl, SITE_B_DQ))) {
-        ok = false;
-        break;
-      }
+    // Phase C of block i: copy this warp's D/2 columns of dQ_i out of TMEM
+    // and release them, then stage them in block i's Q/dO buffers (every MMA
+    // that read Q_i and dO_i is complete: the dq_full arrival follows them)
+    // for the producer's reduce into the fp32 accumulator.  A box is 32 rows
+    // x 32 floats, 128-byte swizzled (16-byte chunk u of row r at chunk
+    // u ^ (r % 8)); rows past L are skipped by the reduce.
+    auto phase_c = [&](int i) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_dq, i & 1, ctl, SITE_B_DQ))) return false;
       tc_fence_after();
+      const int st = i % C::STAGES;
       uint32_t qv[D / 64][32];
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) tmem_ld32(lane_base + C::DP_COL + (D / 2) * h + 32 * c, qv[c]);
@@ -680,6 +706,25 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       fence_proxy_async_smem();  // the producer's reduce reads the stage via the async proxy
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dqst(st));
+      return true;
+    };
+
+    bool ok = true;
+    if constexpr (C::EARLY_S) {
+      // A(0); then per block B(i), A(i+1), C(i): P of the next block is
+      // computed while dK_i and dQ_i run on the tensor core.
+      ok = phase_a(0);
+      for (int i = 0; i < n_i && ok; ++i) {
+        ok = phase_b(i);
+        if (ok && i + 1 < n_i) ok = phase_a(i + 1);
+        if (ok) ok = phase_c(i);
+      }
+    } else {
+      for (int i = 0; i < n_i && ok; ++i) {
+        ok = phase_a(i);
+        if (ok) ok = phase_b(i);
+        if (ok) ok = phase_c(i);
+      }
     }
 
     // Epilogue: the last dq_full arrival came after every MMA of the CTA, so
