@@ -66,26 +66,36 @@ def read_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+# Device-code files each kernel is built from; a profile summary records the
+# hash of these files at capture time and is used only while it matches.
+KERNEL_SOURCES = {
+    "fwd": ["fa_fwd_kernel.cuh", "sm103_ptx.cuh"],
+    "bwd": ["fa_bwd_kernel.cuh", "sm103_ptx.cuh"],
+}
+
+
+def kernel_source_hash(kernel: str = "fwd") -> str:
     h = hashlib.sha256()
-    files = sorted(glob.glob(os.path.join(ROOT, "exact_tiled_attention_09_gb300", "csrc", "*")))
-    for f in files + [os.path.join(ROOT, "include", "fa.h")]:
-        with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "exact_tiled_attention_09_gb300", "csrc", name), "rb") as fh:
+            h.update(name.encode())
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def read_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary of this workload,
-    if it was captured on the current kernel source; else None."""
-    src = kernel_source_hash()
+def read_traffic(workload: str, kernel: str = "fwd"):
+    """DRAM bytes per launch from the committed ncu summary of this kernel on
+    this workload, if it was captured on the current kernel source; else None."""
+    src = kernel_source_hash(kernel)
     for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
         text = open(path).read()
+        m_k = re.search(r"^kernel:\s*(\S+)", text, re.M)
         m_w = re.search(r"^workload:\s*(\S+)", text, re.M)
         m_h = re.search(r"^kernel_source_sha256_16:\s*(\S+)", text, re.M)
         m_t = re.search(r"^dram_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
-        if m_w and m_h and m_t and m_w.group(1) == workload and m_h.group(1) == src:
+        k = m_k.group(1) if m_k else "fwd"
+        if (k == kernel and m_w and m_h and m_t and m_w.group(1) == workload
+                and m_h.group(1) == src):
             return float(m_t.group(1)), os.path.relpath(path, ROOT)
     return None, None
 
@@ -272,9 +282,11 @@ def backward_line(fa, w, t, peaks):
     mean = sum(t) / len(t)
     f = fa.flops_bwd(w.B, w.H, w.L, w.d, w.causal)
     tf = f / (mean * 1e-3) / 1e12
+    traffic, src = read_traffic(w.name, "bwd")
     return {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d, "causal": w.causal,
             "ms_mean": round(mean, 4), "ms_min": round(min(t), 4), "tflops": round(tf, 1),
-            "frac_of_peak": round(tf / peaks["bf16_tflops"], 4), "steps": len(t)}
+            "frac_of_peak": round(tf / peaks["bf16_tflops"], 4), "steps": len(t),
+            "gradient_kernel_dram_bytes": traffic, "traffic_source": src}
 
 
 def splits_for(w, sms):
