@@ -23,7 +23,11 @@ first part, sections 4.1-4.2; chain rule through the scaled scores):
   affordable.
 * :func:`attention_bwd_numpy` -- the same formulas in matrix form.
 
-Parity status: pinned (forward and gradients).  The pins (``tests/test_oracle_pins.py``) check both
+FP8: :mod:`oracle.fp8` holds the E4M3 block quantisation of Q and K
+("FlashAttention 深度解析", third part, section 2.3); the FP8 forward's
+expected result is :func:`attention` on the de-quantised inputs.
+
+Parity status: pinned (forward, gradients, FP8 quantisation).  The pins (``tests/test_oracle_pins.py``) check both
 against the worked example printed on "FlashAttention: как реально
 считается attention на GPU" (section "Код: от игрушечного NumPy до реального
 PyTorch"), against high-precision brute force, closed forms and invariants.
