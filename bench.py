@@ -22,7 +22,9 @@ L=8192 point used for the tensor-core fraction.  ``splitkv`` times the
 split-KV path (split pass + merge) against the single pass on shapes whose
 single-pass grid underfills the GPU.  ``backward`` times the backward pass
 (gradients by recomputation) on every workload: TFLOP/s by the convention
-10*B*H*L^2*d (five L x L x d products; halved when causal).
+10*B*H*L^2*d (five L x L x d products; halved when causal).  ``fp8`` times
+the FP8 forward (E4M3 Q and K with block scales, bf16 V) on every workload
+by the forward's convention, and the block quantisation of Q and K apart.
 
 With more than one GPU (torchrun) every rank runs its own replica of the
 workload (the forward pass has no exchange step); only the timing is
@@ -278,6 +280,37 @@ def time_backward(fa, torch, w, dev, steps, warmup, flush_buf):
     return [s_.elapsed_time(e_) for s_, e_ in ev]
 
 
+def time_fp8(fa, torch, w, dev, steps, warmup, flush_buf):
+    """Per-step device time (ms) of the FP8 forward (``fa.forward_fp8`` on
+    pre-quantised Q and K) and of the quantisation of Q and K; L2 flushed
+    before each step."""
+    q, k, v = device_inputs(w, dev, torch)
+    stream = torch.cuda.current_stream()
+    q8, qs = fa.quantize_fp8(q, stream=stream)
+    k8, ks = fa.quantize_fp8(k, stream=stream)
+    o = torch.empty_like(v)
+    lse = torch.empty((w.B, w.H, w.L), dtype=torch.float32, device=dev)
+    fwd = lambda: fa.forward_fp8(q8, k8, v, qs, ks, scale=w.scale, causal=w.causal, out=o, lse=lse,
+                                 stream=stream)
+    quant = lambda: (fa.quantize_fp8(q, codes=q8, scales=qs, stream=stream),
+                     fa.quantize_fp8(k, codes=k8, scales=ks, stream=stream))
+    out = []
+    for run in (fwd, quant):
+        for _ in range(warmup):
+            run()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for s_, e_ in ev:
+            flush_buf.fill_(1)
+            s_.record(stream)
+            run()
+            e_.record(stream)
+        torch.cuda.synchronize()
+        out.append([s_.elapsed_time(e_) for s_, e_ in ev])
+    return out
+
+
 def backward_line(fa, w, t, peaks):
     mean = sum(t) / len(t)
     f = fa.flops_bwd(w.B, w.H, w.L, w.d, w.causal)
@@ -386,6 +419,7 @@ def run_ours(args):
     extras = []
     splitkv = []
     backward = []
+    fp8 = []
     with ClockSampler(local) as clk:
         if world > 1:
             dist.barrier()
@@ -410,6 +444,15 @@ def run_ours(args):
                                "frac_of_peak": round(tf / peaks["bf16_tflops"], 4),
                                "steps": steps})
                 del qx, kx, vx
+            for name, wx in WORKLOADS.items():
+                steps = max(3, min(args.extra_steps, int(2e13 / wx.flops)))
+                tf8, tq = time_fp8(fa, torch, wx, dev, steps, 3, flush_buf)
+                m8, mq = sum(tf8) / len(tf8), sum(tq) / len(tq)
+                fp8.append({"workload": name, "ms_mean": round(m8, 4), "ms_min": round(min(tf8), 4),
+                            "tflops": round(wx.flops / (m8 * 1e-3) / 1e12, 1),
+                            "frac_of_bf16_peak": round(wx.flops / (m8 * 1e-3) / 1e12
+                                                       / peaks["bf16_tflops"], 4),
+                            "quantize_qk_ms": round(mq, 4), "steps": steps})
             for name, wx in WORKLOADS.items():
                 steps = max(3, min(args.extra_steps,
                                    int(5e13 / fa.flops_bwd(wx.B, wx.H, wx.L, wx.d, wx.causal))))
@@ -484,6 +527,7 @@ def run_ours(args):
             "workloads": extras,
             "splitkv": splitkv,
             "backward": backward,
+            "fp8": fp8,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

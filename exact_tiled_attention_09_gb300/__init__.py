@@ -31,8 +31,8 @@ __all__ = [
     "library", "fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_static", "FA_STATIC_WORKSPACE_BYTES",
     "fa_splitkv_workspace_bytes", "fa_device_status",
     "fa_set_wait_timeout_ns", "fa_test_withhold_q_load", "fa_status_string", "fa_version",
-    "fa_bwd", "fa_bwd_workspace_bytes",
-    "forward", "forward_splitkv", "backward",
+    "fa_bwd", "fa_bwd_workspace_bytes", "fa_quantize_fp8", "fa_fwd_fp8",
+    "forward", "forward_splitkv", "backward", "quantize_fp8", "forward_fp8",
     "flops", "flops_bwd",
 ]
 
@@ -88,6 +88,11 @@ def library() -> ctypes.CDLL:
         lib.fa_bwd.restype = ci
         lib.fa_bwd_workspace_bytes.argtypes = [ci, ci, ci, ci]
         lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.fa_quantize_fp8.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp]
+        lib.fa_quantize_fp8.restype = ci
+        lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ctypes.c_float, ci,
+                                   vp]
+        lib.fa_fwd_fp8.restype = ci
         lib.fa_version.argtypes = []
         lib.fa_version.restype = ci
         _lib = lib
@@ -131,6 +136,17 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, L, d, scale, causal, workspa
 
 def fa_bwd_workspace_bytes(B, H, L, d) -> int:
     return library().fa_bwd_workspace_bytes(B, H, L, d)
+
+
+def fa_quantize_fp8(x, codes, scales, B, H, L, d, stream) -> int:
+    """Direct call of the FP8 block quantisation with integer addresses."""
+    return library().fa_quantize_fp8(x, codes, scales, B, H, L, d, stream)
+
+
+def fa_fwd_fp8(q8, k8, v, q_scale, k_scale, o, lse, B, H, L, d, scale, causal, stream) -> int:
+    """Direct call of the FP8 forward with integer addresses."""
+    return library().fa_fwd_fp8(q8, k8, v, q_scale, k_scale, o, lse, B, H, L, d, scale, causal,
+                                stream)
 
 
 def fa_device_status(stream=None, clear=True) -> int:
@@ -283,3 +299,61 @@ def backward(q, k, v, o, lse, do, scale=None, causal=False, dq=None, dk=None, dv
     if rc != FA_OK:
         raise FAError(rc, "fa_bwd")
     return dq, dk, dv
+
+
+def quantize_fp8(x, codes=None, scales=None, stream=None):
+    """E4M3 block quantisation of a CUDA bf16 tensor [B, H, L, d]: returns
+    (codes uint8 [B, H, L, d], scales fp32 [B, H, ceil(L/128)])."""
+    import torch
+
+    if x.dim() != 4 or x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA bf16 tensor [B, H, L, d]")
+    B, H, L, d = x.shape
+    nb = (L + 127) // 128
+    if codes is None:
+        codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((B, H, nb), dtype=torch.float32, device=x.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    with torch.cuda.device(x.device):
+        rc = fa_quantize_fp8(x.data_ptr(), codes.data_ptr(), scales.data_ptr(), B, H, L, d,
+                             stream.cuda_stream)
+    if rc != FA_OK:
+        raise FAError(rc, "fa_quantize_fp8")
+    return codes, scales
+
+
+def forward_fp8(q8, k8, v, q_scale, k_scale, scale=None, causal=False, out=None, lse=None,
+                stream=None):
+    """Attention forward with E4M3 Q and K (codes and block scales from
+    :func:`quantize_fp8`) and bf16 V; returns (o bf16, lse fp32)."""
+    import torch
+
+    if q8.shape != k8.shape or q8.shape != v.shape or q8.dim() != 4:
+        raise ValueError("q8, k8, v must share one shape [B, H, L, d]")
+    if q8.dtype != torch.uint8 or k8.dtype != torch.uint8 or v.dtype != torch.bfloat16:
+        raise ValueError("q8, k8 must be uint8 codes and v bf16")
+    for t in (q8, k8, v, q_scale, k_scale):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+    B, H, L, d = v.shape
+    nb = (L + 127) // 128
+    for t in (q_scale, k_scale):
+        if t.shape != (B, H, nb) or t.dtype != torch.float32:
+            raise ValueError("scales must be fp32 [B, H, ceil(L/128)]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(v)
+    if lse is None:
+        lse = torch.empty((B, H, L), dtype=torch.float32, device=v.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(v.device)
+    with torch.cuda.device(v.device):
+        rc = fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v.data_ptr(), q_scale.data_ptr(),
+                        k_scale.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, L, d,
+                        float(scale), int(bool(causal)), stream.cuda_stream)
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd_fp8")
+    return out, lse

@@ -11,6 +11,7 @@
 
 #include "fa.h"
 #include "fa_bwd_kernel.cuh"
+#include "fa_fp8.cuh"
 #include "fa_fwd_kernel.cuh"
 #include "fa_merge.cuh"
 
@@ -62,6 +63,24 @@ bool encode_map(CUtensorMap* map, const void* ptr, int BH, int L, int D) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// E4M3 codes [BH, L, D] (one byte each) as a 3-D tensor (D, L, BH) with a
+// D x 128 x 1 box: one box per 128-row tile, rows of D bytes, 128-byte
+// swizzle at D = 128 and 64-byte swizzle at D = 64 (the layouts the FP8
+// MMA descriptors read).
+bool encode_map_u8(CUtensorMap* map, const void* ptr, int BH, int L, int D) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L) * D};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(BLOCK_N), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The fp32 dQ accumulator [BH, L, D] as a 3-D tensor (D, L, BH) with a
 // 32 x 32 x 1 box (128-byte rows) and the 128-byte swizzle: the target of
 // the backward kernel's reduce-adds.  Rows past L inside a head are out of
@@ -93,11 +112,11 @@ bool configure_once(Kernel kernel, int smem, int dev, bool* configured, std::mut
   return true;
 }
 
-template <int D, bool CAUSAL, bool SPLIT>
+template <int D, bool CAUSAL, bool SPLIT, bool FP8 = false>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
            const FwdArgs& args, int n_splits, cudaStream_t stream, int dev) {
-  auto kernel = fa_fwd_kernel<D, CAUSAL, SPLIT>;
-  constexpr int smem = FwdCfg<D>::SMEM_BYTES;
+  auto kernel = fa_fwd_kernel<D, CAUSAL, SPLIT, FP8>;
+  constexpr int smem = FwdCfg<D, FP8>::SMEM_BYTES;
   static bool configured[kMaxDevices] = {};
   static std::mutex mu;
   if (!configure_once(kernel, smem, dev, configured, mu)) return FA_ERR_LAUNCH;
@@ -173,6 +192,9 @@ int prepare(const void* q, const void* k, const void* v, void* o, float* lse, in
     args.group_heads = static_cast<int>(g < 1 ? 1 : (g > BH ? BH : g));
   }
   args.scale_log2 = scale * 1.4426950408889634f;
+  args.q_scale = nullptr;
+  args.k_scale = nullptr;
+  args.n_blocks = static_cast<int>((static_cast<int64_t>(L) + BLOCK_N - 1) / BLOCK_N);
   args.status = status;
   args.timeout_ns = g_timeout_ns;
   args.test_withhold_q = g_test_withhold_q;
@@ -448,6 +470,54 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
                 : launch_bwd<128, false>(mq, mk, mv, mdo, mdq, args, pre, dq16, s, dev);
 }
 
+int fa_quantize_fp8(const void* x, void* codes, float* scales, int B, int H, int L, int d,
+                    fa_stream_t stream) {
+  using namespace fa;
+  if (!x || !codes || !scales || B < 1 || H < 1 || L < 1) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  const int64_t nb = (static_cast<int64_t>(L) + 127) / 128;
+  if (BH * nb > 0x7fffffff) return FA_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(scales, 4)) return FA_ERR_MISALIGNED;
+  int dev = -1, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_DEVICE;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return FA_ERR_DEVICE;
+  if (major != 10 || minor != 3) return FA_ERR_DEVICE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const dim3 grid(static_cast<unsigned>(BH * nb));
+  const uint16_t* xs = static_cast<const uint16_t*>(x);
+  uint8_t* cs = static_cast<uint8_t*>(codes);
+  if (d == 64)
+    fa_quantize_fp8_kernel<64><<<grid, QUANT_THREADS, 0, s>>>(xs, cs, scales, L, static_cast<int>(nb));
+  else
+    fa_quantize_fp8_kernel<128><<<grid, QUANT_THREADS, 0, s>>>(xs, cs, scales, L, static_cast<int>(nb));
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int fa_fwd_fp8(const void* q8, const void* k8, const void* v, const float* q_scale,
+               const float* k_scale, void* o, float* lse, int B, int H, int L, int d, float scale,
+               int causal, fa_stream_t stream) {
+  using namespace fa;
+  if (!q_scale || !k_scale) return FA_ERR_INVALID_ARG;
+  if (!aligned(q_scale, 4) || !aligned(k_scale, 4)) return FA_ERR_MISALIGNED;
+  Prepared p;
+  const int rc = prepare(q8, k8, v, o, lse, B, H, L, d, scale, causal, &p);
+  if (rc != FA_OK) return rc;
+  // Q and K are E4M3 codes: one-byte tensor maps in place of the bf16 ones.
+  if (!encode_map_u8(&p.mq, q8, p.args.bh, L, d) || !encode_map_u8(&p.mk, k8, p.args.bh, L, d))
+    return FA_ERR_LAUNCH;
+  p.args.q_scale = q_scale;
+  p.args.k_scale = k_scale;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (d == 64)
+    return causal ? launch<64, true, false, true>(p.mq, p.mk, p.mv, p.args, 1, s, p.dev)
+                  : launch<64, false, false, true>(p.mq, p.mk, p.mv, p.args, 1, s, p.dev);
+  return causal ? launch<128, true, false, true>(p.mq, p.mk, p.mv, p.args, 1, s, p.dev)
+                : launch<128, false, false, true>(p.mq, p.mk, p.mv, p.args, 1, s, p.dev);
+}
+
 int fa_device_status(fa_stream_t stream, int clear) {
   using namespace fa;
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -478,6 +548,6 @@ const char* fa_status_string(int status) {
   }
 }
 
-int fa_version(void) { return 200; }
+int fa_version(void) { return 300; }
 
 }  // extern "C"

@@ -76,14 +76,21 @@ enum : uint32_t {
   SITE_DRAIN = 7,
 };
 
-template <int D>
+template <int D, bool FP8 = false>
 struct FwdCfg {
   static_assert(D == 64 || D == 128, "head dimension must be 64 or 128");
   static constexpr int BOXES = D / 64;
-  static constexpr int TILE_BYTES = BLOCK_N * D * 2;
+  static constexpr int TILE_BYTES = BLOCK_N * D * 2;  // a bf16 tile (V; Q, K unless FP8)
   static constexpr int NSLOT = (D == 64) ? 8 : 4;
+  // Q and K tiles: bf16 as D/64 boxes of 64 columns, or with FP8 one box of
+  // 128 rows x D bytes (E4M3 codes; 128-byte swizzle at D = 128, 64-byte at
+  // D = 64).
+  static constexpr int QK_BOXES = FP8 ? 1 : BOXES;
+  static constexpr int QK_BOX_BYTES = FP8 ? BLOCK_N * D : BOX_BYTES;
+  static constexpr int QK_BOX_COLS = FP8 ? D : 64;
+  static constexpr int QK_TILE_BYTES = FP8 ? BLOCK_N * D : TILE_BYTES;
   static constexpr int Q_OFF = NSLOT * TILE_BYTES;
-  static constexpr int BAR_OFF = Q_OFF + TILES_PER_CTA * TILE_BYTES;
+  static constexpr int BAR_OFF = Q_OFF + TILES_PER_CTA * QK_TILE_BYTES;
   // q_full, full[NSLOT], empty[NSLOT], s_full[2], p_full[2], o_done[2], drain
   static constexpr int NBAR = 1 + 2 * NSLOT + 2 + 2 + 2 + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
@@ -108,6 +115,10 @@ struct FwdArgs {
   int bh;             // B * H
   int group_heads;    // heads per scheduling group (see the CTA order)
   float scale_log2;   // scale * log2(e)
+  // FP8 only: fp32 scales of the 128-row blocks of Q and K, [BH, n_blocks]
+  const float* q_scale;
+  const float* k_scale;
+  int n_blocks;       // ceil(L / 128)
   unsigned int* status;
   unsigned long long timeout_ns;
   int test_withhold_q;  // test hook: skip the Q copy so the first MMA wait runs out
@@ -127,18 +138,23 @@ __device__ __forceinline__ int blocks_for_tile(int row0, int L) {
 // (split + 1) * blocks_per_split) of its rows and writes fp32 partial results
 // (Flash-Decoding's per-chunk pass, "04 Transformers, Attention, and
 // FlashAttention", Flash-Decoding); the merge kernel finishes them.
-template <int D, bool CAUSAL, bool SPLIT>
+//
+// FP8: Q and K are E4M3 codes with one fp32 scale per 128-row block ("FlashAttention
+// 深度解析", third part, section 2.3: Q_FP8 = Quantize(Q_block / s_q), S =
+// Q_FP8 K_FP8^T * s_q * s_k); S comes from a kind::f8f6f4 MMA, and s_q * s_k
+// joins the softmax multiplier of each block.  P and V stay bf16.
+template <int D, bool CAUSAL, bool SPLIT, bool FP8 = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - raw);
 
   const uint32_t ring = base;
-  const uint32_t sQ = base + C::Q_OFF;  // tile t at sQ + t * TILE_BYTES
+  const uint32_t sQ = base + C::Q_OFF;  // tile t at sQ + t * QK_TILE_BYTES
   const uint32_t bars = base + C::BAR_OFF;
   const uint32_t bar_q = bars;
   auto bar_full = [&](int s) { return bars + 8u * (1 + s); };
@@ -230,24 +246,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------ producer
     if (!args.test_withhold_q && elect_one()) {
-      mbar_arrive_expect_tx(bar_q, TILES_PER_CTA * C::TILE_BYTES);
+      mbar_arrive_expect_tx(bar_q, TILES_PER_CTA * C::QK_TILE_BYTES);
       for (int t = 0; t < TILES_PER_CTA; ++t)
-        for (int c = 0; c < C::BOXES; ++c)
-          tma_load_3d(sQ + t * C::TILE_BYTES + c * BOX_BYTES, &tmQ, bar_q, c * 64,
-                      row_base + t * BLOCK_M, bh);
+        for (int c = 0; c < C::QK_BOXES; ++c)
+          tma_load_3d(sQ + t * C::QK_TILE_BYTES + c * C::QK_BOX_BYTES, &tmQ, bar_q,
+                      c * C::QK_BOX_COLS, row_base + t * BLOCK_M, bh);
     }
     __syncwarp();
     int cnt = 0;
     bool ok = true;
-    auto load = [&](const CUtensorMap* map, int j) -> bool {
+    auto load = [&](const CUtensorMap* map, int j, bool is_k) -> bool {
       const int s = cnt % C::NSLOT;
       const uint32_t use = static_cast<uint32_t>(cnt / C::NSLOT);
       if (!warp_wait(bar_empty(s), (use & 1u) ^ 1u, SITE_EMPTY)) return false;
       if (elect_one()) {
-        mbar_arrive_expect_tx(bar_full(s), C::TILE_BYTES);
+        const int boxes = is_k ? C::QK_BOXES : C::BOXES;
+        const int box_bytes = is_k ? C::QK_BOX_BYTES : BOX_BYTES;
+        const int box_cols = is_k ? C::QK_BOX_COLS : 64;
+        mbar_arrive_expect_tx(bar_full(s), is_k ? C::QK_TILE_BYTES : C::TILE_BYTES);
         const uint32_t dst = ring + s * C::TILE_BYTES;
-        for (int c = 0; c < C::BOXES; ++c)
-          tma_load_3d(dst + c * BOX_BYTES, map, bar_full(s), c * 64, (jb + j) * BLOCK_N, bh);
+        for (int c = 0; c < boxes; ++c)
+          tma_load_3d(dst + c * box_bytes, map, bar_full(s), c * box_cols, (jb + j) * BLOCK_N,
+                      bh);
       }
       __syncwarp();
       ++cnt;
@@ -256,8 +276,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // Ring positions: K_j at 2j, V_j at 2j + 1 (the MMA warp's first uses
     // come in this order).
     for (int j = 0; j < n_blk && ok; ++j) {
-      ok = load(&tmK, j);
-      if (ok) ok = load(&tmV, j);
+      ok = load(&tmK, j, true);
+      if (ok) ok = load(&tmV, j, false);
     }
     if (!ok && lane == 0) {
       // Let every copy already issued land before the CTA exits.
@@ -288,13 +308,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
     };
     auto issue_s = [&](int t, uint32_t kaddr) {
-      const uint32_t q = sQ + t * C::TILE_BYTES;
+      const uint32_t q = sQ + t * C::QK_TILE_BYTES;
       if (elect_one()) {
+        if constexpr (FP8) {
+          // 32 codes (32 bytes) per step along rows of D bytes
+          constexpr uint32_t IDESC_S8 = idesc_e4m3_f32(BLOCK_M, BLOCK_N);
+          constexpr uint32_t SWZ = (D == 128) ? 2u : 4u;     // 128- or 64-byte rows
+          constexpr uint32_t SBO = (D == 128) ? 1024u : 512u;  // 8-row atom
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
-          mma_ss(tmem + C::S_COL(t), sdesc_sw128(q + off, 16, 1024),
-                 sdesc_sw128(kaddr + off, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 32; ++kk)
+            mma_ss_f8(tmem + C::S_COL(t), sdesc_swz(q + kk * 32, 16, SBO, SWZ),
+                      sdesc_swz(kaddr + kk * 32, 16, SBO, SWZ), IDESC_S8, kk > 0 ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
+            mma_ss(tmem + C::S_COL(t), sdesc_sw128(q + off, 16, 1024),
+                   sdesc_sw128(kaddr + off, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+          }
         }
         mma_commit(bar_s(t));
       }
@@ -362,13 +393,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int tile_row0 = row_base + t * BLOCK_M;
     const int q_row = tile_row0 + row;
     const int n_my = t == 0 ? n_blk0 : n_blk1;
-    const float sl2 = args.scale_log2;
-    const bool pos_scale = sl2 > 0.f;
+    float sl2 = args.scale_log2;  // FP8: times s_q * s_k of the block, set per block
+    const bool pos_scale = args.scale_log2 > 0.f;  // the block scales are positive
     float m = -INFINITY;  // running max of scale*log2e*s
     float l = 0.f;        // running sum of P~ relative to m
     bool ok = true;
+    float sq = 1.f;
+    if constexpr (FP8)
+      if (n_my > 0) sq = args.q_scale[static_cast<size_t>(bh) * args.n_blocks + tile_row0 / BLOCK_M];
 
     for (int j = 0; j < n_my; ++j) {
+      if constexpr (FP8)
+        sl2 = args.scale_log2 * sq * args.k_scale[static_cast<size_t>(bh) * args.n_blocks + jb + j];
       const bool w = mbar_wait(bar_s(t), j & 1, ctl, SITE_S);
       if (!__all_sync(0xffffffffu, w)) {
         ok = false;

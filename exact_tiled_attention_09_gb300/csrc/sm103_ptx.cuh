@@ -212,6 +212,18 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T with 8-bit floating-point operands
+// (kind::f8f6f4; the formats come from the instruction descriptor).
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation issued so far by this
 // thread has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -346,6 +358,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The same with an explicit swizzle mode in bits 61-63: 2 = 128-byte rows,
+// 4 = 64-byte rows (atoms of 8 rows x 64 bytes).
+__device__ __forceinline__ uint64_t sdesc_swz(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t mode) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  d |= static_cast<uint64_t>(mode & 7u) << 61;
+  return d;
+}
+
 // Instruction descriptor for kind::f16 with bf16 A and B and an fp32
 // accumulator: D format (bits 4-5) = 1 (f32), A format (bits 7-9) = 1 (bf16),
 // B format (bits 10-12) = 1 (bf16), A major (bit 15), B major (bit 16;
@@ -361,6 +386,21 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32_ab(uint32_t M, uint32_t N,
                                                          bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn_major ? (1u << 15) : 0u) |
          (b_mn_major ? (1u << 16) : 0u) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// Instruction descriptor for kind::f8f6f4 with E4M3 A and B (format code 0
+// in bits 7-9 and 10-12), an fp32 accumulator (bits 4-5 = 1), both operands
+// K-major, N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
+  return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// Two floats -> two E4M3 codes (round to nearest even, saturating to
+// +-448); `lo` in bits 0..7.
+__device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 }  // namespace fa

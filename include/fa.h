@@ -147,6 +147,44 @@ int fa_fwd_splitkv_static(const void *q, const void *k, const void *v, void *o, 
                           fa_stream_t stream);
 
 /*
+ * fa_quantize_fp8 -- FP8 (E4M3) block quantisation of Q or K for
+ * fa_fwd_fp8 ("FlashAttention 深度解析", third part, section 2.3: each block
+ * gets s = max|block| / FP8_MAX and is stored as Quantize(block / s)).
+ *
+ *   x      : device bf16 [B, H, L, d], layout as for fa_fwd; 16-byte aligned.
+ *   codes  : device output, one byte per element [B, H, L, d] (E4M3: sign,
+ *            4 exponent bits with bias 7, 3 mantissa bits); 16-byte aligned.
+ *   scales : device output fp32 [B, H, ceil(L / 128)]: the scale of each
+ *            block of 128 consecutive rows of a head, amax / 448 (correctly
+ *            rounded fp32 division), or 1 for a block of zeros.
+ *
+ * codes = x / s (correctly rounded fp32 division), rounded to the nearest
+ * E4M3 value (ties to even) and saturated to +-448.  Asynchronous on
+ * `stream`; errors as for fa_fwd (d = 64 or 128); nothing is launched on an
+ * error.
+ */
+int fa_quantize_fp8(const void *x, void *codes, float *scales, int B, int H, int L, int d,
+                    fa_stream_t stream);
+
+/*
+ * fa_fwd_fp8 -- fa_fwd with Q and K in FP8: S = (Q_FP8 K_FP8^T) * s_q * s_k
+ * * scale (the same page and section), P and V in bf16 as in fa_fwd.
+ *
+ *   q8, k8          : E4M3 codes and their block scales from fa_quantize_fp8
+ *   q_scale, k_scale  (codes 16-byte aligned, scales 4-byte aligned).
+ *   v, o, lse, B..causal, stream : as for fa_fwd.
+ *
+ * The S product runs on the 8-bit tensor-core path (tcgen05 kind::f8f6f4,
+ * fp32 accumulation); s_q * s_k join the softmax's scale per block.  The
+ * result is exact attention of the de-quantised Q and K (codes times their
+ * block scale) with V, within the tolerances of fa_fwd.  Errors: those of
+ * fa_fwd, plus FA_ERR_INVALID_ARG / FA_ERR_MISALIGNED for the scale arrays.
+ */
+int fa_fwd_fp8(const void *q8, const void *k8, const void *v, const float *q_scale,
+               const float *k_scale, void *o, float *lse, int B, int H, int L, int d,
+               float scale, int causal, fa_stream_t stream);
+
+/*
  * fa_bwd_workspace_bytes -- bytes of workspace fa_bwd needs for these sizes:
  * 256-byte-aligned room for an fp32 dQ accumulator [B, H, L, d] and two fp32
  * per-query arrays [B, H, Lp] (Lp = L rounded up to a multiple of 128).

@@ -214,3 +214,28 @@ def test_python_backward_rejects_bad_tensors():
     lse = torch.zeros(1, 1, 8)
     with pytest.raises(ValueError):
         fa.backward(q, q, q, q, lse, q)  # CPU tensors
+
+
+# ---------------------------------------------------------------- FP8
+def test_fp8_validation_launches_nothing(lib):
+    q = dict(x=0x10000, codes=0x20000, scales=0x30000)
+    call_q = lambda **o: fa.fa_quantize_fp8(o.get("x", q["x"]), o.get("codes", q["codes"]),
+                                            o.get("scales", q["scales"]), 1, 2, o.get("L", 300),
+                                            o.get("d", 64), None)
+    assert call_q(x=0) == fa.FA_ERR_INVALID_ARG
+    assert call_q(L=0) == fa.FA_ERR_INVALID_ARG
+    assert call_q(d=96) == fa.FA_ERR_UNSUPPORTED_D
+    assert call_q(codes=0x20008) == fa.FA_ERR_MISALIGNED
+    assert call_q(scales=0x30002) == fa.FA_ERR_MISALIGNED
+    f = lambda qs=0x40000, ks=0x50000, **o: fa.fa_fwd_fp8(
+        o.get("q8", 0x10000), 0x20000, 0x30000, qs, ks, 0x60000, 0x70000, 1, 2,
+        o.get("L", 300), o.get("d", 128), 0.1, 0, None)
+    assert f(qs=0) == fa.FA_ERR_INVALID_ARG
+    assert f(ks=0) == fa.FA_ERR_INVALID_ARG
+    assert f(qs=0x40002) == fa.FA_ERR_MISALIGNED
+    assert f(q8=0) == fa.FA_ERR_INVALID_ARG
+    assert f(d=32) == fa.FA_ERR_UNSUPPORTED_D
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        assert call_q() == fa.FA_ERR_DEVICE
+        assert f() == fa.FA_ERR_DEVICE
