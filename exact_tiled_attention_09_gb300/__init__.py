@@ -32,6 +32,7 @@ __all__ = [
     "fa_splitkv_workspace_bytes", "fa_device_status",
     "fa_set_wait_timeout_ns", "fa_test_withhold_q_load", "fa_status_string", "fa_version",
     "fa_bwd", "fa_bwd_workspace_bytes", "fa_quantize_fp8", "fa_fwd_fp8",
+    "fa_fwd_host", "fa_fwd_host_workspace_bytes", "forward_host",
     "forward", "forward_splitkv", "backward", "quantize_fp8", "forward_fp8",
     "flops", "flops_bwd",
 ]
@@ -93,6 +94,11 @@ def library() -> ctypes.CDLL:
         lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ctypes.c_float, ci,
                                    vp]
         lib.fa_fwd_fp8.restype = ci
+        lib.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ctypes.c_float, ci, vp,
+                                    ctypes.c_size_t, vp]
+        lib.fa_fwd_host.restype = ci
+        lib.fa_fwd_host_workspace_bytes.argtypes = [ci, ci, ci, ci]
+        lib.fa_fwd_host_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_version.argtypes = []
         lib.fa_version.restype = ci
         _lib = lib
@@ -147,6 +153,17 @@ def fa_fwd_fp8(q8, k8, v, q_scale, k_scale, o, lse, B, H, L, d, scale, causal, s
     """Direct call of the FP8 forward with integer addresses."""
     return library().fa_fwd_fp8(q8, k8, v, q_scale, k_scale, o, lse, B, H, L, d, scale, causal,
                                 stream)
+
+
+def fa_fwd_host(q, k, v, o, lse, B, H, L, d, scale, causal, workspace, workspace_bytes,
+                stream) -> int:
+    """Direct call of the host-buffer forward with integer addresses."""
+    return library().fa_fwd_host(q, k, v, o, lse, B, H, L, d, scale, causal, workspace,
+                                 workspace_bytes, stream)
+
+
+def fa_fwd_host_workspace_bytes(B, H, L, d) -> int:
+    return library().fa_fwd_host_workspace_bytes(B, H, L, d)
 
 
 def fa_device_status(stream=None, clear=True) -> int:
@@ -356,4 +373,41 @@ def forward_fp8(q8, k8, v, q_scale, k_scale, scale=None, causal=False, out=None,
                         float(scale), int(bool(causal)), stream.cuda_stream)
     if rc != FA_OK:
         raise FAError(rc, "fa_fwd_fp8")
+    return out, lse
+
+
+def forward_host(q, k, v, scale=None, causal=False, out=None, lse=None, workspace=None,
+                 stream=None, device=None):
+    """:func:`forward` on CPU tensors: copies in, forward, copies out, all on
+    ``stream`` (asynchronous when the tensors are pinned; synchronise the
+    stream before reading ``out``/``lse``).  ``workspace`` is a CUDA uint8
+    tensor of at least ``fa_fwd_host_workspace_bytes`` bytes."""
+    import torch
+
+    if q.shape != k.shape or q.shape != v.shape or q.dim() != 4:
+        raise ValueError("q, k, v must share one shape [B, H, L, d]")
+    for t in (q, k, v):
+        if t.dtype != torch.bfloat16 or t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous CPU bfloat16 tensors")
+    B, H, L, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    need = fa_fwd_host_workspace_bytes(B, H, L, d)
+    if need == 0:
+        raise ValueError("invalid sizes")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, L), dtype=torch.float32)
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    with torch.cuda.device(device):
+        rc = fa_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                         B, H, L, d, float(scale), int(bool(causal)), workspace.data_ptr(),
+                         workspace.numel() * workspace.element_size(), stream.cuda_stream)
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd_host")
     return out, lse

@@ -518,6 +518,69 @@ int fa_fwd_fp8(const void* q8, const void* k8, const void* v, const float* q_sca
                 : launch<128, false, false, true>(p.mq, p.mk, p.mv, p.args, 1, s, p.dev);
 }
 
+size_t fa_fwd_host_workspace_bytes(int B, int H, int L, int d) {
+  if (B < 1 || H < 1 || L < 1 || (d != 64 && d != 128)) return 0;
+  const size_t n = static_cast<size_t>(B) * H * L * d * 2;  // bytes of one bf16 tensor
+  return fa::align256(4 * n) + static_cast<size_t>(B) * H * L * 4;
+}
+
+int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int L, int d, float scale, int causal, void* workspace, size_t workspace_bytes,
+                fa_stream_t stream) {
+  using namespace fa;
+  if (!q || !k || !v || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
+  const size_t need = fa_fwd_host_workspace_bytes(B, H, L, d);
+  if (need == 0) return (d != 64 && d != 128 && B >= 1 && H >= 1 && L >= 1)
+                            ? FA_ERR_UNSUPPORTED_D : FA_ERR_INVALID_ARG;
+  if (workspace_bytes < need) return FA_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return FA_ERR_MISALIGNED;
+  const size_t n = static_cast<size_t>(B) * H * L * d * 2;
+  const size_t nl = static_cast<size_t>(B) * H * L * 4;
+  char* ws = static_cast<char*>(workspace);
+  // device copies: Q, K, V, O back to back, then LSE
+  char* dq = ws;
+  char* dk = ws + n;
+  char* dv = ws + 2 * n;
+  char* dout = ws + 3 * n;
+  float* dlse = reinterpret_cast<float*>(ws + align256(4 * n));
+  // Validate every argument (with the device buffers) before any copy.
+  Prepared p;
+  int rc = prepare(dq, dk, dv, dout, dlse, B, H, L, d, scale, causal, &p);
+  if (rc != FA_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const char* hq = static_cast<const char*>(q);
+  const char* hk = static_cast<const char*>(k);
+  const char* hv = static_cast<const char*>(v);
+  // inputs adjacent in host memory travel in one copy (the device copies are)
+  if (hk == hq + n && hv == hk + n) {
+    if (cudaMemcpyAsync(dq, hq, 3 * n, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return FA_ERR_LAUNCH;
+  } else {
+    if (cudaMemcpyAsync(dq, hq, n, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(dk, hk, n, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(dv, hv, n, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return FA_ERR_LAUNCH;
+  }
+  if (d == 64)
+    rc = causal ? launch<64, true, false>(p.mq, p.mk, p.mv, p.args, 1, s, p.dev)
+                : launch<64, false, false>(p.mq, p.mk, p.mv, p.args, 1, s, p.dev);
+  else
+    rc = causal ? launch<128, true, false>(p.mq, p.mk, p.mv, p.args, 1, s, p.dev)
+                : launch<128, false, false>(p.mq, p.mk, p.mv, p.args, 1, s, p.dev);
+  if (rc != FA_OK) return rc;
+  char* ho = static_cast<char*>(o);
+  char* hl = reinterpret_cast<char*>(lse);
+  if (hl == ho + n && reinterpret_cast<char*>(dlse) == dout + n) {
+    if (cudaMemcpyAsync(ho, dout, n + nl, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      return FA_ERR_LAUNCH;
+  } else {
+    if (cudaMemcpyAsync(ho, dout, n, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyAsync(hl, dlse, nl, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      return FA_ERR_LAUNCH;
+  }
+  return FA_OK;
+}
+
 int fa_device_status(fa_stream_t stream, int clear) {
   using namespace fa;
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)

@@ -147,6 +147,40 @@ int fa_fwd_splitkv_static(const void *q, const void *k, const void *v, void *o, 
                           fa_stream_t stream);
 
 /*
+ * fa_fwd_host_workspace_bytes -- device workspace fa_fwd_host needs: room for
+ * device copies of Q, K, V and O (bf16, back to back) and LSE (fp32),
+ * 256-byte aligned.  Returns 0 for invalid sizes.  Host only.
+ */
+size_t fa_fwd_host_workspace_bytes(int B, int H, int L, int d);
+
+/*
+ * fa_fwd_host -- fa_fwd on HOST buffers: copies q, k, v to the device,
+ * runs the forward, copies o and lse back, all asynchronous on `stream`.
+ *
+ *   q, k, v : host bf16 [B, H, L, d] (layout as for fa_fwd).  Inputs that lie
+ *             back to back in host memory (k == q + size, v == k + size)
+ *             travel in one copy.
+ *   o, lse  : host outputs; o and lse back to back travel in one copy.
+ *   workspace : device scratch of fa_fwd_host_workspace_bytes(B, H, L, d)
+ *             bytes or more, 256-byte aligned; its contents on entry do not
+ *             matter.
+ *   other arguments as for fa_fwd.
+ *
+ * For the copies to be asynchronous (and to overlap with other work) the
+ * host buffers must be page-locked; pageable buffers work but the copies
+ * then block the calling thread.  The outputs are valid once `stream` has
+ * reached the end of the call.  Calls on different streams with different
+ * workspaces may overlap (one call's copies with another's kernel); calls
+ * sharing a workspace on concurrent streams race.  Errors: those of fa_fwd,
+ * plus FA_ERR_INVALID_ARG for a null or too-small workspace and
+ * FA_ERR_MISALIGNED for a workspace not 256-byte aligned; nothing is copied
+ * or launched on a validation error.
+ */
+int fa_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                int L, int d, float scale, int causal, void *workspace, size_t workspace_bytes,
+                fa_stream_t stream);
+
+/*
  * fa_quantize_fp8 -- FP8 (E4M3) block quantisation of Q or K for
  * fa_fwd_fp8 ("FlashAttention 深度解析", third part, section 2.3: each block
  * gets s = max|block| / FP8_MAX and is stored as Quantize(block / s)).

@@ -239,3 +239,21 @@ def test_fp8_validation_launches_nothing(lib):
     if not torch.cuda.is_available():
         assert call_q() == fa.FA_ERR_DEVICE
         assert f() == fa.FA_ERR_DEVICE
+
+
+def test_host_forward_validation_launches_nothing(lib):
+    n = fa.fa_fwd_host_workspace_bytes(1, 2, 300, 64)
+    assert n == ((4 * 1 * 2 * 300 * 64 * 2 + 255) // 256) * 256 + 1 * 2 * 300 * 4
+    assert fa.fa_fwd_host_workspace_bytes(1, 2, 300, 96) == 0
+    call = lambda ws=0x1000000, wsb=n, **o: fa.fa_fwd_host(
+        o.get("q", 0x10000), 0x20000, 0x30000, 0x40000, 0x50000, 1, 2, o.get("L", 300),
+        o.get("d", 64), 0.125, 0, ws, wsb, None)
+    assert call(q=0) == fa.FA_ERR_INVALID_ARG
+    assert call(ws=0) == fa.FA_ERR_INVALID_ARG
+    assert call(wsb=n - 1) == fa.FA_ERR_INVALID_ARG
+    assert call(ws=0x1000010) == fa.FA_ERR_MISALIGNED
+    assert call(d=96) == fa.FA_ERR_UNSUPPORTED_D
+    assert call(L=0) == fa.FA_ERR_INVALID_ARG
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        assert call() == fa.FA_ERR_DEVICE
