@@ -74,6 +74,7 @@ def read_peaks():
 # hash of these files at capture time and is used only while it matches.
 KERNEL_SOURCES = {
     "fwd": ["fa_fwd_kernel.cuh", "sm103_ptx.cuh"],
+    "fwd_fp8": ["fa_fwd_kernel.cuh", "sm103_ptx.cuh"],
     "bwd": ["fa_bwd_kernel.cuh", "sm103_ptx.cuh"],
 }
 
@@ -472,7 +473,9 @@ def run_ours(args):
                 steps = max(3, min(args.extra_steps, int(2e13 / wx.flops)))
                 tf8, tq = time_fp8(fa, torch, wx, dev, steps, 3, flush_buf)
                 m8, mq = sum(tf8) / len(tf8), sum(tq) / len(tq)
+                tr8, tr8_src = read_traffic(name, "fwd_fp8")
                 fp8.append({"workload": name, "ms_mean": round(m8, 4), "ms_min": round(min(tf8), 4),
+                            "attention_kernel_dram_bytes": tr8, "traffic_source": tr8_src,
                             "tflops": round(wx.flops / (m8 * 1e-3) / 1e12, 1),
                             "frac_of_bf16_peak": round(wx.flops / (m8 * 1e-3) / 1e12
                                                        / peaks["bf16_tflops"], 4),
@@ -586,6 +589,27 @@ def run_profile_bwd(args):
     print(json.dumps({"backward": backward_line(fa, w, t, peaks)}), flush=True)
 
 
+def run_profile_fp8(args):
+    """Time only the FP8 forward of one workload (for profiler captures)."""
+    import torch
+
+    import exact_tiled_attention_09_gb300 as fa
+    from fa_inputs import WORKLOADS
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fa.library()
+    w = WORKLOADS[args.profile_fp8]
+    flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    t8, tq = time_fp8(fa, torch, w, dev, args.steps, args.warmup, flush_buf)
+    if fa.fa_device_status(None, clear=True) != fa.FA_OK:
+        raise RuntimeError("a kernel wait timed out during the benchmark")
+    m8 = sum(t8) / len(t8)
+    print(json.dumps({"fp8": {"workload": w.name, "ms_mean": round(m8, 4),
+                              "tflops": round(w.flops / (m8 * 1e-3) / 1e12, 1),
+                              "quantize_qk_ms": round(sum(tq) / len(tq), 4)}}), flush=True)
+
+
 def run_reference(args):
     """The fp64 oracle on the host cores, same metric/config (rank 0 only)."""
     rank = int(os.environ.get("RANK", "0"))
@@ -642,10 +666,14 @@ def main():
     ap.add_argument("--profile-bwd", metavar="WORKLOAD", default=None,
                     help="time only the backward pass of WORKLOAD and print its line "
                          "(for profiler captures; not the benchmark line)")
+    ap.add_argument("--profile-fp8", metavar="WORKLOAD", default=None,
+                    help="time only the FP8 forward of WORKLOAD (for profiler captures)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.profile_bwd:
         run_profile_bwd(args)
+    elif args.profile_fp8:
+        run_profile_fp8(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
