@@ -406,6 +406,23 @@ def time_e2e(fa, torch, host, w, steps, warmup, flush_buf, dev):
     return pipe, serial, 3 * nb, nb + lb
 
 
+def max_over_ranks(values, world, dist=None, device=None):
+    """Element-wise max of per-rank timing totals across the process group
+    (the slowest rank sets the job's time); identity for one rank."""
+    if world <= 1:
+        return list(values)
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def whole_job_tflops(world, flops_per_step, steps, total_ms):
+    """TFLOP/s of the whole job: every rank runs ``steps`` steps of its own
+    replica, and the job takes the slowest rank's time."""
+    return world * flops_per_step * steps / (total_ms * 1e-3) / 1e12
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -505,15 +522,10 @@ def run_ours(args):
     if fa.fa_device_status(None, clear=True) != fa.FA_OK:
         raise RuntimeError("a kernel wait timed out during the benchmark")
 
-    total_ms = sum(ms)
-    total_e2e = sum(e2e_ms)
-    if world > 1:
-        t = torch.tensor([total_ms, total_e2e], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, total_e2e = float(t[0]), float(t[1])
+    total_ms, total_e2e = max_over_ranks([sum(ms), sum(e2e_ms)], world, dist, dev)
     flops_step = w.flops
-    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
-    e2e_value = world * flops_step * args.steps / (total_e2e * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops_step, args.steps, total_ms)
+    e2e_value = whole_job_tflops(world, flops_step, args.steps, total_e2e)
     mean_launch_ms = sum(ms) / len(ms)
     achieved = flops_step / (mean_launch_ms * 1e-3) / 1e12
     traffic, traffic_src = read_traffic(w.name)
