@@ -473,11 +473,14 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     // scores-like products: A and B K-major tiles of this CTA, K = d
     auto issue_kmajor = [&](uint32_t dcol, uint32_t a, uint32_t b, uint32_t bar) {
       if (elect_one()) {
+        // descriptors built once; a step moves the start-address field by
+        // off / 16 (no carry out of the field inside shared memory)
+        const uint64_t ad = sdesc_sw128(a, 16, 1024);
+        const uint64_t bd = sdesc_sw128(b, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * BOX + (kk & 3) * 32;
-          mma_ss(tmem + dcol, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(b + off, 16, 1024), ID_S,
-                 kk > 0 ? 1u : 0u);
+          mma_ss(tmem + dcol, ad + (off >> 4), bd + (off >> 4), ID_S, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar);
       }
@@ -511,10 +514,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       if (elect_one()) {
+        const uint64_t dod = sdesc_sw128(sdO(st), BOX, 1024);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_ts(tmem + C::DV_COL, tmem + C::S_COL + 64 * (kk >> 2) + 8 * (kk & 3),
-                 sdesc_sw128(sdO(st) + kk * 2048, BOX, 1024), ID_DV, (i > 0 || kk > 0) ? 1u : 0u);
+                 dod + kk * (2048 >> 4), ID_DV, (i > 0 || kk > 0) ? 1u : 0u);
       }
       __syncwarp();
       if (C::EARLY_S && i + 1 < n_i) {
@@ -526,14 +530,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       if (elect_one()) {
+        const uint64_t dsk = sdesc_sw128(sDS, 16, 1024);     // dS^T, K-major
+        const uint64_t dsm = sdesc_sw128(sDS, BOX, 1024);    // the same tile, MN-major
+        const uint64_t qmn = sdesc_sw128(sQ(st), BOX, 1024);
+        const uint64_t kmn = sdesc_sw128(sK, BOX, 1024);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + C::DK_COL, sdesc_sw128(sDS + (kk >> 2) * BOX + (kk & 3) * 32, 16, 1024),
-                 sdesc_sw128(sQ(st) + kk * 2048, BOX, 1024), ID_DK, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_ss(tmem + C::DK_COL, dsk + (((kk >> 2) * BOX + (kk & 3) * 32) >> 4),
+                 qmn + kk * (2048 >> 4), ID_DK, (i > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + C::DP_COL, sdesc_sw128(sDS + kk * 2048, BOX, 1024),
-                 sdesc_sw128(sK + kk * 2048, BOX, 1024), ID_DQ, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + C::DP_COL, dsm + kk * (2048 >> 4), kmn + kk * (2048 >> 4), ID_DQ,
+                 kk > 0 ? 1u : 0u);
         mma_commit(bar_dq);
       }
       __syncwarp();

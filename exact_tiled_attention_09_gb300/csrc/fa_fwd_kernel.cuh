@@ -315,16 +315,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           constexpr uint32_t IDESC_S8 = idesc_e4m3_f32(BLOCK_M, BLOCK_N);
           constexpr uint32_t SWZ = (D == 128) ? 2u : 4u;     // 128- or 64-byte rows
           constexpr uint32_t SBO = (D == 128) ? 1024u : 512u;  // 8-row atom
+          const uint64_t qd = sdesc_swz(q, 16, SBO, SWZ);
+          const uint64_t kd = sdesc_swz(kaddr, 16, SBO, SWZ);
 #pragma unroll
           for (int kk = 0; kk < D / 32; ++kk)
-            mma_ss_f8(tmem + C::S_COL(t), sdesc_swz(q + kk * 32, 16, SBO, SWZ),
-                      sdesc_swz(kaddr + kk * 32, 16, SBO, SWZ), IDESC_S8, kk > 0 ? 1u : 0u);
+            mma_ss_f8(tmem + C::S_COL(t), qd + kk * (32 >> 4), kd + kk * (32 >> 4), IDESC_S8,
+                      kk > 0 ? 1u : 0u);
         } else {
+          // Descriptors built once; a k-step moves the start-address field
+          // (address / 16, bits 0-13) by off / 16, which never carries out
+          // of the field inside shared memory.
+          const uint64_t qd = sdesc_sw128(q, 16, 1024);
+          const uint64_t kd = sdesc_sw128(kaddr, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
-            mma_ss(tmem + C::S_COL(t), sdesc_sw128(q + off, 16, 1024),
-                   sdesc_sw128(kaddr + off, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+            mma_ss(tmem + C::S_COL(t), qd + (off >> 4), kd + (off >> 4), IDESC_S,
+                   kk > 0 ? 1u : 0u);
           }
         }
         mma_commit(bar_s(t));
@@ -335,10 +342,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!warp_wait(bar_p(t), j & 1, SITE_P)) return false;
       tc_fence_after();
       if (elect_one()) {
+        const uint64_t vd = sdesc_sw128(vaddr, BOX_BYTES, 1024);
 #pragma unroll
         for (int kk = 0; kk < BLOCK_N / 16; ++kk) {
-          mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + kk * 8,
-                 sdesc_sw128(vaddr + kk * 2048, BOX_BYTES, 1024), IDESC_O,
+          mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + kk * 8, vd + kk * (2048 >> 4), IDESC_O,
                  (j > 0 || kk > 0) ? 1u : 0u);
         }
         if (j == n_t(t) - 1) mma_commit(bar_o(t));
