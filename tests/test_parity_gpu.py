@@ -135,6 +135,29 @@ def test_increasing_max_forces_every_rescale(dev):
         _full_parity(dev, qb, kb, vb, 1.0, causal, f"growing max causal={causal}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_max_growth_around_the_rescale_threshold(dev, d):
+    # Row r's score for key j is a_r * c * j with a_r from 0.2 to 1.0: per
+    # block of 128 keys the max grows by up to ~5.8 powers of two, so rows
+    # keep a stale reference (P~ above 1) for a block or two and then
+    # rescale, each at its own block; a warp mixes rows that need the
+    # rescale with rows that do not.
+    L = 1000
+    per_block = 5.8 / math.log2(math.e)           # score growth per block
+    q = np.zeros((1, 2, L, d), np.float32)
+    q[..., 0] = np.linspace(0.2, 1.0, L)
+    k = np.zeros((1, 2, L, d), np.float32)
+    k[..., 0] = np.arange(L) * (per_block / 128.0)
+    rng = np.random.default_rng(17)
+    q[..., 1:] = 0.05 * rng.standard_normal((1, 2, L, d - 1))
+    k[..., 1:] = 0.05 * rng.standard_normal((1, 2, L, d - 1))
+    v = rng.standard_normal((1, 2, L, d)).astype(np.float32)
+    from fa_inputs import round_to_bf16_bits
+    qb, kb, vb = (round_to_bf16_bits(x) for x in (q, k, v))
+    for causal in (False, True):
+        _full_parity(dev, qb, kb, vb, 1.0, causal, f"threshold growth d={d} causal={causal}")
+
+
 # ------------------------------------------------------------------ invariants
 def test_causal_first_row_is_v0_exactly(dev):
     qb, kb, vb = make_custom(2, 3, 300, 128, seed=31)
