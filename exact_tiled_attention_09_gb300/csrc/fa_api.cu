@@ -122,7 +122,7 @@ int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
   if (!configure_once(kernel, smem, dev, configured, mu)) return FA_ERR_LAUNCH;
   const dim3 grid(static_cast<unsigned>(args.n_ctiles) * static_cast<unsigned>(args.bh) *
                   static_cast<unsigned>(n_splits));
-  kernel<<<grid, NUM_THREADS, smem, stream>>>(mq, mk, mv, args);
+  kernel<<<grid, FwdCfg<D, FP8>::THREADS, smem, stream>>>(mq, mk, mv, args);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

@@ -10,9 +10,10 @@
 // "FlashAttention 深度解析", third part, section 2.2 describes for Hopper,
 // re-targeted here to tcgen05 and tensor memory).
 //
-// Warp roles (320 threads):
+// Warp roles (320 threads; 352 at d = 64):
 //   warp 0      MMA issuer and owner of the tensor memory: all 32 lanes run
 //               the loop and poll the barriers, one elected lane issues
+//               (d = 64: the products of Q tile 0 only)
 //   warp 1      TMA producer (same scheme): loads Q0 and Q1 once, then K_j
 //               and V_j tiles into a ring of shared-memory slots (full/empty
 //               mbarriers)
@@ -20,6 +21,7 @@
 //               touch lanes 32*(w%4) .. 32*(w%4)+31, so the four warps of a
 //               group cover quarters 2, 3, 0, 1)
 //   warps 6..9  softmax of Q tile 1
+//   warp 10     d = 64 only: MMA issuer of Q tile 1
 //
 // MMA order per K/V block j (each S_t buffer holds P_t after the softmax, so
 // S_t of block j+1 is issued only after O_t += P_t V_j of block j):
@@ -30,6 +32,15 @@
 // block j+1 also proves O_t += P_t V_j finished, so the softmax may rescale
 // O_t right away.
 //
+// d = 64 differs: P_t has tensor-memory columns of its own, so S_t of block
+// j+1 is issued as soon as the softmax has read S_t of block j (s_free), and
+// each tile has its own MMA warp, so neither tile's products wait behind the
+// other's barriers.  The softmax computes block j's exponentials in
+// registers, then waits for O_t += P_t V_{j-1} (o_done, committed after
+// every PV at d = 64) before writing P_t and rescaling O_t; the tile runs
+// from block to block without waiting for the tensor core.  Both MMA warps
+// release every ring slot (empty barriers count 2).
+//
 // Softmax per block (per row): scores s -> mask -> m_new = max(m, rowmax)
 // (in units of scale*log2(e)) -> P~ = exp2(s*scale*log2e - m_new) written as
 // bf16 over the first 64 columns of its S buffer -> l = c*l + rowsum(P~) and
@@ -38,6 +49,7 @@
 //
 // Tensor memory (512 columns x 128 lanes of 32 bits):
 //   [0,128) S0/P0   [128,256) S1/P1   [256,256+D) O0   [256+D,256+2D) O1
+//   d = 64: P0 at [384,448) and P1 at [448,512) instead (bf16, two per column)
 //
 // Shared memory (1024-byte aligned): NSLOT ring slots, then Q0 and Q1, then
 // the mbarriers.  Every tile is stored as D/64 boxes of 128 rows x 64 columns
@@ -58,8 +70,9 @@ constexpr int BLOCK_M = 128;          // rows per Q tile (one TMEM lane each)
 constexpr int BLOCK_N = 128;          // keys per K/V block
 constexpr int TILES_PER_CTA = 2;
 constexpr int ROWS_PER_CTA = BLOCK_M * TILES_PER_CTA;
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_THREADS = 320;  // d = 128; d = 64 adds a second MMA warp
 constexpr int MMA_WARP = 0;
+constexpr int MMA_WARP_T1 = 10;  // d = 64: the MMA warp of Q tile 1
 constexpr int PRODUCER_WARP = 1;
 constexpr int FIRST_SOFTMAX_WARP = 2;
 constexpr uint32_t TMEM_COLS = 512;
@@ -89,10 +102,15 @@ struct FwdCfg {
   static constexpr int QK_BOX_BYTES = FP8 ? BLOCK_N * D : BOX_BYTES;
   static constexpr int QK_BOX_COLS = FP8 ? D : 64;
   static constexpr int QK_TILE_BYTES = FP8 ? BLOCK_N * D : TILE_BYTES;
+  // d = 64: P_t gets tensor-memory columns of its own, S_t is free as soon
+  // as the softmax has read it, and each Q tile has its own MMA warp.
+  static constexpr bool SPLIT_P = (D == 64);
+  static constexpr int THREADS = SPLIT_P ? NUM_THREADS + 32 : NUM_THREADS;
   static constexpr int Q_OFF = NSLOT * TILE_BYTES;
   static constexpr int BAR_OFF = Q_OFF + TILES_PER_CTA * QK_TILE_BYTES;
-  // q_full, full[NSLOT], empty[NSLOT], s_full[2], p_full[2], o_done[2], drain
-  static constexpr int NBAR = 1 + 2 * NSLOT + 2 + 2 + 2 + 1;
+  // q_full, full[NSLOT], empty[NSLOT], s_full[2], p_full[2], o_done[2],
+  // drain[2] (one per MMA warp), s_free[2]
+  static constexpr int NBAR = 1 + 2 * NSLOT + 2 + 2 + 2 + 2 + 2;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + alignment slack
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -100,6 +118,10 @@ struct FwdCfg {
   __host__ __device__ static constexpr uint32_t O_COL(int t) {
     return 256u + static_cast<uint32_t>(D) * t;
   }
+  __host__ __device__ static constexpr uint32_t P_COL(int t) {
+    return SPLIT_P ? 384u + 64u * t : S_COL(t);
+  }
+  static_assert(!SPLIT_P || 384 + 2 * 64 <= 512, "tensor memory budget");
 };
 
 struct FwdArgs {
@@ -144,7 +166,7 @@ __device__ __forceinline__ int blocks_for_tile(int row0, int L) {
 // Q_FP8 K_FP8^T * s_q * s_k); S comes from a kind::f8f6f4 MMA, and s_q * s_k
 // joins the softmax multiplier of each block.  P and V stay bf16.
 template <int D, bool CAUSAL, bool SPLIT, bool FP8 = false>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
   using C = FwdCfg<D, FP8>;
@@ -162,7 +184,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto bar_s = [&](int t) { return bars + 8u * (1 + 2 * C::NSLOT + t); };
   auto bar_p = [&](int t) { return bars + 8u * (3 + 2 * C::NSLOT + t); };
   auto bar_o = [&](int t) { return bars + 8u * (5 + 2 * C::NSLOT + t); };
-  const uint32_t bar_drain = bars + 8u * (7 + 2 * C::NSLOT);
+  auto bar_drain = [&](int t) { return bars + 8u * (7 + 2 * C::NSLOT + t); };
+  auto bar_sfree = [&](int t) { return bars + 8u * (9 + 2 * C::NSLOT + t); };
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + C::MISC_OFF);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::MISC_OFF + 4);
 
@@ -208,14 +231,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(bar_q, 1);
     for (int s = 0; s < C::NSLOT; ++s) {
       mbar_init(bar_full(s), 1);
-      mbar_init(bar_empty(s), 1);
+      mbar_init(bar_empty(s), C::SPLIT_P ? 2 : 1);  // d = 64: both MMA warps release
     }
     for (int t = 0; t < TILES_PER_CTA; ++t) {
       mbar_init(bar_s(t), 1);
       mbar_init(bar_p(t), 4);  // one arrival per softmax warp
       mbar_init(bar_o(t), 1);
     }
-    mbar_init(bar_drain, 1);
+    for (int t = 0; t < TILES_PER_CTA; ++t) {
+      mbar_init(bar_drain(t), 1);
+      mbar_init(bar_sfree(t), 4);  // one arrival per softmax warp
+    }
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -275,8 +301,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     };
     // Ring positions: K_j at 2j, V_j at 2j + 1 (the MMA warp's first uses
     // come in this order).
+    // Q and block 0 go out first; the rest of the ring waits until Q has
+    // landed, so that on a short, cold launch (every CTA loading from DRAM
+    // at once) the first score products are not queued behind K/V blocks
+    // needed later.
     for (int j = 0; j < n_blk && ok; ++j) {
-      ok = load(&tmK, j, true);
+      if (j == 1 && !args.test_withhold_q) ok = warp_wait(bar_q, 0, SITE_Q);
+      if (ok) ok = load(&tmK, j, true);
       if (ok) ok = load(&tmV, j, false);
     }
     if (!ok && lane == 0) {
@@ -287,7 +318,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (issued > 0) mbar_wait_drain(bar_full(s), (issued - 1) & 1, args.timeout_ns);
       }
     }
-  } else if (warp == MMA_WARP) {
+  } else if (warp == MMA_WARP || (C::SPLIT_P && warp == MMA_WARP_T1)) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t IDESC_S = idesc_bf16_f32(BLOCK_M, BLOCK_N, false);
     constexpr uint32_t IDESC_O = idesc_bf16_f32(BLOCK_M, D, true);
@@ -345,16 +376,70 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint64_t vd = sdesc_sw128(vaddr, BOX_BYTES, 1024);
 #pragma unroll
         for (int kk = 0; kk < BLOCK_N / 16; ++kk) {
-          mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + kk * 8, vd + kk * (2048 >> 4), IDESC_O,
+          mma_ts(tmem + C::O_COL(t), tmem + C::P_COL(t) + kk * 8, vd + kk * (2048 >> 4), IDESC_O,
                  (j > 0 || kk > 0) ? 1u : 0u);
         }
-        if (j == n_t(t) - 1) mma_commit(bar_o(t));
+        // With its own P columns the softmax waits for every PV (it rewrites
+        // P_t and may rescale O_t next block); otherwise only the epilogue.
+        if (C::SPLIT_P || j == n_t(t) - 1) mma_commit(bar_o(t));
       }
       __syncwarp();
       return true;
     };
 
     uint32_t kaddr = 0, vaddr = 0;
+    if constexpr (C::SPLIT_P) {
+      // d = 64: this warp issues only tile t's products.  Per block j:
+      // S_t of block j+1 as soon as the softmax has read S_t of block j
+      // (s_free), then O_t += P_t V_j when P_t is ready.  Every ring position
+      // is released by both MMA warps (count 2): a commit where this warp's
+      // MMAs read the slot, a plain arrival where tile t had no use for it,
+      // always after the slot was seen full.
+      const int t = warp == MMA_WARP ? 0 : 1;
+      const int n_mine = n_t(t);
+      auto release_t = [&](int pos, bool used) {
+        if (elect_one()) {
+          if (used)
+            mma_commit(bar_empty(pos % C::NSLOT));
+          else
+            mbar_arrive(bar_empty(pos % C::NSLOT));
+        }
+        __syncwarp();
+      };
+      if (ok && n_blk > 0) {
+        ok = acquire(0, kaddr);
+        if (ok) {
+          if (n_mine > 0) issue_s(t, kaddr);
+          release_t(0, n_mine > 0);
+        }
+      }
+      for (int j = 0; j < n_blk && ok; ++j) {
+        if (j + 1 < n_blk) {
+          ok = acquire(2 * j + 2, kaddr);
+          const bool use_k = j + 1 < n_mine;
+          if (ok && use_k) {
+            ok = warp_wait(bar_sfree(t), j & 1, SITE_S);
+            if (ok) {
+              tc_fence_after();
+              issue_s(t, kaddr);
+            }
+          }
+          if (ok) release_t(2 * j + 2, use_k);
+        }
+        if (ok) ok = acquire(2 * j + 1, vaddr);
+        const bool use_v = j < n_mine;
+        if (ok && use_v) ok = issue_pv(t, j, vaddr);
+        if (ok) release_t(2 * j + 1, use_v);
+      }
+      if (!ok) {
+        // Every MMA this warp issued must finish before the tensor memory is freed.
+        if (elect_one()) {
+          mma_commit(bar_drain(t));
+          mbar_wait_drain(bar_drain(t), 0, args.timeout_ns);
+        }
+        __syncwarp();
+      }
+    } else {
     if (ok && n_blk > 0) {
       ok = acquire(0, kaddr);
       if (ok) {
@@ -384,11 +469,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (!ok) {
       // Every MMA already issued must finish before the tensor memory is freed.
       if (elect_one()) {
-        mma_commit(bar_drain);
-        mbar_wait_drain(bar_drain, 0, args.timeout_ns);
+        mma_commit(bar_drain(0));
+        mbar_wait_drain(bar_drain(0), 0, args.timeout_ns);
       }
       __syncwarp();
     }
+    }  // one MMA warp for both tiles (d = 128)
   } else {
     // ------------------------------------------------------------ softmax
     const int t = (warp - FIRST_SOFTMAX_WARP) >> 2;  // Q tile of this warpgroup
@@ -424,6 +510,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tmem_wait_ld();
 #pragma unroll
       for (int c = 0; c < 4; ++c) reg_fence32(sr[c]);
+      if constexpr (C::SPLIT_P) {
+        // The scores are in registers: S_t may take the next block's product.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_sfree(t));
+      }
 
       // Masks: keys past the end of the sequence; causal keys after the query.
       const int k0 = (jb + j) * BLOCK_N;
@@ -442,17 +534,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // Row max in units of scale*log2(e).
       float blk;
       if (pos_scale) {
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        // eight independent chains of 8 three-way maxima (short latency)
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            mx[0] = fmax3(mx[0], __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
-            mx[1] = fmax3(mx[1], __uint_as_float(sr[c][e + 2]), __uint_as_float(sr[c][e + 3]));
-            mx[2] = fmax3(mx[2], __uint_as_float(sr[c][e + 4]), __uint_as_float(sr[c][e + 5]));
-            mx[3] = fmax3(mx[3], __uint_as_float(sr[c][e + 6]), __uint_as_float(sr[c][e + 7]));
-          }
-        blk = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]) * sl2;
+          for (int e = 0; e < 32; e += 16)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              mx[i] = fmax3(mx[i], __uint_as_float(sr[c][e + 2 * i]),
+                            __uint_as_float(sr[c][e + 2 * i + 1]));
+        blk = fmaxf(fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), mx[6]), mx[7]) *
+              sl2;
       } else {
         // scale <= 0: work on x = scale*log2e*s directly (masked stays -inf).
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -481,10 +576,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint64_t mul2 = f2_pack(mul, mul);
       const uint64_t negm2 = f2_pack(-m, -m);
       uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
-      // Keys 32c..32c+31 pack into columns 16c..16c+15 of the S buffer.
+      // Keys 32c..32c+31 pack into columns 16c..16c+15 of the P columns.
+      // With separate P columns the stores wait until O_t += P_t V_{j-1}
+      // has completed (it reads the same columns); the exponentials run
+      // first, so that wait overlaps them.
+      uint32_t pk[4][16];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           float x0, x1;
@@ -494,17 +592,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const float p0 = ex2_approx(x0);
           const float p1 = ex2_approx(x1);
           sum2[(e >> 1) & 3] = f2_add(sum2[(e >> 1) & 3], f2_pack(p0, p1));
-          pk[e >> 1] = pack_bf16x2(p0, p1);
+          pk[c][e >> 1] = pack_bf16x2(p0, p1);
         }
-        tmem_st16(lane_base + s_col + 16u * c, pk);
+        if constexpr (!C::SPLIT_P) tmem_st16(lane_base + C::P_COL(t) + 16u * c, pk[c]);
+      }
+      if constexpr (C::SPLIT_P) {
+        if (j > 0) {
+          // P_t and O_t are free once O_t += P_t V_{j-1} has completed.
+          const bool wo = mbar_wait(bar_o(t), (j - 1) & 1, ctl, SITE_O);
+          if (!__all_sync(0xffffffffu, wo)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_st16(lane_base + C::P_COL(t) + 16u * c, pk[c]);
       }
       float s_lo, s_hi;
       f2_unpack(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), s_lo, s_hi);
       const float rowsum = s_lo + s_hi;
       l = (j == 0) ? rowsum : fmaf(corr, l, rowsum);
 
-      // O_t is quiescent here: the arrival on s_full for this block came
-      // after O_t += P_t V_{j-1} completed, and the next PV waits for p_full.
+      // O_t is quiescent here: O_t += P_t V_{j-1} has completed (with separate
+      // P columns the o_done wait above says so; otherwise the arrival on
+      // s_full for this block came after it), and the next PV waits for p_full.
       if (__any_sync(0xffffffffu, grew)) {
         // All of O_t's columns in one round trip: issue every load, wait
         // once, scale in packed pairs, store back.
@@ -540,7 +652,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const bool store = q_row < L;
     if (ok && n_my > 0) {
       // Epilogue: wait for the last O_t += P_t V, then O / l and LSE.
-      const bool w = mbar_wait(bar_o(t), 0, ctl, SITE_O);
+      const bool w = mbar_wait(bar_o(t), C::SPLIT_P ? (n_my - 1) & 1 : 0, ctl, SITE_O);
       if (__all_sync(0xffffffffu, w)) {
         tc_fence_after();
         const float inv_l = 1.f / l;
