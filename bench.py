@@ -83,12 +83,38 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(src: str) -> str:
+    """C++ source with comments removed and whitespace runs collapsed, so that
+    editing a comment does not change the kernel's source hash.  String and
+    character literals (the inline PTX) are kept verbatim."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash(kernel: str = "fwd") -> str:
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "exact_tiled_attention_09_gb300", "csrc", name), "rb") as fh:
+        with open(os.path.join(ROOT, "exact_tiled_attention_09_gb300", "csrc", name),
+                  encoding="utf-8") as fh:
             h.update(name.encode())
-            h.update(fh.read())
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

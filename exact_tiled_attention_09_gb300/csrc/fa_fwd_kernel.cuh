@@ -23,8 +23,8 @@
 //   warps 6..9  softmax of Q tile 1
 //   warp 10     d = 64 only: MMA issuer of Q tile 1
 //
-// MMA order per K/V block j (each S_t buffer holds P_t after the softmax, so
-// S_t of block j+1 is issued only after O_t += P_t V_j of block j):
+// d = 128, MMA order per K/V block j (each S_t buffer holds P_t after the
+// softmax, so S_t of block j+1 is issued only after O_t += P_t V_j):
 //   PV0_j, S0_{j+1}, PV1_j, S1_{j+1}
 // The tensor core therefore computes PV1_j and S1_{j+1} while softmax 0
 // works on S0_{j+1}, and the other way round.  Because tcgen05 operations of
@@ -43,7 +43,8 @@
 //
 // Softmax per block (per row): scores s -> mask -> m_new = max(m, rowmax)
 // (in units of scale*log2(e)) -> P~ = exp2(s*scale*log2e - m_new) written as
-// bf16 over the first 64 columns of its S buffer -> l = c*l + rowsum(P~) and
+// bf16 over the first 64 columns of its S buffer (d = 64: into P_t's own
+// columns) -> l = c*l + rowsum(P~) and
 // O *= c with c = exp2(m - m_new) whenever the max grew (a warp skips the O
 // pass when no row of it changed: c is then exactly 1).
 //
