@@ -25,11 +25,23 @@ def test_literals_are_kept_verbatim():
     assert out.endswith(";")
 
 
-def test_every_committed_summary_matches_the_current_kernels():
-    # each summary's DRAM bytes are reported only while its hash matches
-    for workload, kernel in [("B4_H8_L1024_d64", "fwd"), ("gate_B1_H32_L8192_d128", "fwd"),
-                             ("B1_H16_L32768_d64", "fwd"), ("gate_B1_H32_L8192_d128", "bwd"),
-                             ("B1_H16_L32768_d64", "bwd"), ("gate_B1_H32_L8192_d128", "fwd_fp8")]:
+def test_committed_summaries_carry_the_lookup_fields():
+    # every summary names its kernel, workload, code hash and DRAM bytes; its
+    # bytes are reported only while the hash matches the current kernel code
+    import glob
+    import os
+    import re
+    paths = sorted(glob.glob(os.path.join(bench.ROOT, "profiles", "*.md")))
+    assert paths
+    for path in paths:
+        text = open(path).read()
+        fields = {k: re.search(rf"^{k}:\s*(\S+)", text, re.M)
+                  for k in ("kernel", "workload", "kernel_source_sha256_16", "dram_bytes_per_launch")}
+        assert all(fields.values()), path
+        kernel, workload = fields["kernel"].group(1), fields["workload"].group(1)
+        assert kernel in bench.KERNEL_SOURCES, path
         traffic, src = bench.read_traffic(workload, kernel)
-        assert traffic is not None and traffic > 0, (workload, kernel)
-        assert src.startswith("profiles/")
+        if fields["kernel_source_sha256_16"].group(1) == bench.kernel_source_hash(kernel):
+            assert traffic == float(fields["dram_bytes_per_launch"].group(1)) and src
+        else:
+            assert traffic is None or src != os.path.relpath(path, bench.ROOT)
