@@ -40,8 +40,9 @@
 //               (its keys) and query columns 64*h..64*h+63, h = (w-2)/4
 //
 // Tensor memory (512 columns): [0,128) S^T, then P^T as packed bf16 (half
-// h's 64 queries in columns 64h..64h+31); [128,256) dP^T, then dQ_i;
-// [256,256+D) dV_j; [256+D,256+2D) dK_j.
+// h's 64 queries in columns 64h..64h+31); [128,256) dP^T, then dQ_i
+// (d = 128; at d = 64 dQ_i has [384,448) of its own, so dP_{i+1} need not
+// wait for dQ_i to be copied out); [256,256+D) dV_j; [256+D,256+2D) dK_j.
 //
 // Order of the MMAs per query block (tcgen05 operations of one thread
 // complete in issue order, which the hand-offs rely on):
@@ -133,6 +134,12 @@ struct BwdCfg {
   static constexpr uint32_t DP_COL = 128;
   static constexpr uint32_t DV_COL = 256;
   static constexpr uint32_t DK_COL = 256 + D;
+  // d = 64 leaves 128 tensor-memory columns free: dQ_i gets its own 64, so
+  // dP_{i+1} need not wait until dQ_i has been copied out (at d = 128 dQ_i
+  // reuses dP_i's columns).
+  static constexpr bool SPLIT_DQ = (D == 64);
+  static constexpr uint32_t DQ_COL = SPLIT_DQ ? 256 + 2 * D : DP_COL;
+  static_assert(!SPLIT_DQ || DQ_COL + D <= 512, "tensor memory budget");
 };
 
 struct BwdArgs {
@@ -501,7 +508,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     }
     for (int i = 0; i < n_i && ok; ++i) {
       const int st = i % C::STAGES;
-      if (i > 0) {
+      if (i > 0 && !C::SPLIT_DQ) {
+        // dP_i goes into the columns dQ_{i-1} occupies until copied out
         ok = warp_wait(bar_dqfree, (i - 1) & 1, SITE_B_DQFREE);
         if (!ok) break;
       }
@@ -528,6 +536,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       // dK += dS^T Q_i and dQ_i = dS K_j once dS^T is in shared memory.
       ok = warp_wait(bar_ds, i & 1, SITE_B_DS);
       if (!ok) break;
+      if (C::SPLIT_DQ && i > 0) {
+        // dQ_i goes into the columns of dQ_{i-1}: copied out by now?
+        ok = warp_wait(bar_dqfree, (i - 1) & 1, SITE_B_DQFREE);
+        if (!ok) break;
+      }
       tc_fence_after();
       if (elect_one()) {
         const uint64_t dsk = sdesc_sw128(sDS, 16, 1024);     // dS^T, K-major
@@ -540,7 +553,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                  qmn + kk * (2048 >> 4), ID_DK, (i > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + C::DP_COL, dsm + kk * (2048 >> 4), kmn + kk * (2048 >> 4), ID_DQ,
+          mma_ss(tmem + C::DQ_COL, dsm + kk * (2048 >> 4), kmn + kk * (2048 >> 4), ID_DQ,
                  kk > 0 ? 1u : 0u);
         mma_commit(bar_dq);
       }
@@ -696,7 +709,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const int st = i % C::STAGES;
       uint32_t qv[D / 64][32];
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) tmem_ld32(lane_base + C::DP_COL + (D / 2) * h + 32 * c, qv[c]);
+      for (int c = 0; c < D / 64; ++c) tmem_ld32(lane_base + C::DQ_COL + (D / 2) * h + 32 * c, qv[c]);
       tmem_wait_ld();
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) reg_fence32(qv[c]);
