@@ -175,37 +175,6 @@ struct BwdPreArgs {
   float scale;
 };
 
-// 2^x for a pair of floats on the FMA pipe instead of the MUFU unit, which
-// the recomputation of P otherwise saturates (one ex2 per score, 16 per
-// clock per SM).  Range reduction to the nearest integer: t = x + 1.5*2^23
-// rounds x to an integer n held in t's low mantissa bits, f = x - n lies in
-// [-1/2, 1/2], and 2^x = 2^f * 2^n is p(f) with n added to its exponent
-// field ((bits(t) << 23) mod 2^32 == n << 23).  p is the cubic minimax fit
-// of 2^f in relative error on [-1/2, 1/2] (Remez exchange; coefficients
-// from exp2_poly_fit.py, which prints them), max relative error 7.5e-5 in
-// fp32 -- far below the 2^-9 of the bf16 rounding that P undergoes.  x is
-// clamped to -126 first, so -inf and deep underflow give tiny positive
-// values, never NaN.
-constexpr float EXP2_C0 = 0.9999280571937561f;
-constexpr float EXP2_C1 = 0.6932609677314758f;
-constexpr float EXP2_C2 = 0.2426111251115799f;
-constexpr float EXP2_C3 = 0.0551716685295105f;
-
-__device__ __forceinline__ void exp2_fma_pair(float x0, float x1, float& y0, float& y1) {
-  const uint64_t x = f2_pack(fmaxf(x0, -126.f), fmaxf(x1, -126.f));
-  const uint64_t t = f2_add(x, f2_pack(12582912.f, 12582912.f));
-  const uint64_t n = f2_add(t, f2_pack(-12582912.f, -12582912.f));
-  const uint64_t f = f2_fma(n, f2_pack(-1.f, -1.f), x);
-  uint64_t q = f2_fma(f, f2_pack(EXP2_C3, EXP2_C3), f2_pack(EXP2_C2, EXP2_C2));
-  q = f2_fma(q, f, f2_pack(EXP2_C1, EXP2_C1));
-  q = f2_fma(q, f, f2_pack(EXP2_C0, EXP2_C0));
-  float q0, q1, t0, t1;
-  f2_unpack(q, q0, q1);
-  f2_unpack(t, t0, t1);
-  y0 = __uint_as_float(__float_as_uint(q0) + (__float_as_uint(t0) << 23));
-  y1 = __uint_as_float(__float_as_uint(q1) + (__float_as_uint(t1) << 23));
-}
-
 constexpr int BWD_AUX_WARPS = 8;  // rows per block of the pre-pass
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -621,9 +590,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][e + 2]), __uint_as_float(sr[c][e + 3])),
                              sl2x2, f2_pack(a.z, a.w)),
                       x2, x3);
-            // half of the exponentials on the MUFU unit, half on the FMA pipe
-            float pe[4] = {ex2_approx(x0), ex2_approx(x1), 0.f, 0.f};
-            exp2_fma_pair(x2, x3, pe[2], pe[3]);
+            float pe[4] = {ex2_approx(x0), ex2_approx(x1), ex2_approx(x2), ex2_approx(x3)};
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               // causal: key r > query (64h + 32c + e + u) of the same block;
