@@ -285,7 +285,7 @@ void fa_set_wait_timeout_ns(uint64_t ns);
 /*
  * fa_test_withhold_q_load -- test hook for the timeout path.  While enabled
  * (nonzero), the forward kernels launched afterwards skip their Q copy and
- * the backward kernel its K/V copy, so the MMA warp's first wait never
+ * the backward kernel its K/V copy, so the first wait on that copy never
  * completes: it gives up after the wait limit, every role stops and drains,
  * the tensor memory is freed and fa_device_status reports FA_ERR_TIMEOUT.
  * Outputs of such launches are undefined.  Process-wide; leave at 0 outside
