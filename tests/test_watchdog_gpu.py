@@ -46,7 +46,8 @@ def _f64(bits):
     return bf16_bits_to_float32(bits).astype(np.float64)
 
 
-@pytest.mark.parametrize("d,causal,split", [(64, False, 0), (128, True, 0), (128, False, 3)])
+@pytest.mark.parametrize("d,causal,split", [(64, False, 0), (64, True, 3), (128, True, 0),
+                                           (128, False, 3)])
 def test_wait_that_runs_out_is_reported_and_the_context_survives(dev, d, causal, split):
     import torch
     B, H, L = 2, 3, 600
