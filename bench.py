@@ -3,10 +3,11 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 One step = one attention forward (the whole hot path, one kernel launch) over
-the headline workload B=4, H=8, L=1024, d=64, non-causal, scale 1/8, inputs
-Q, K, V ~ N(0,1) drawn by the seeded generator and rounded to bf16.  The
-inputs are resident in HBM when timing starts; they fit in L2, so L2 is
-flushed (a 512 MiB write) before every timed step, outside the timed events.
+the headline workload B=1, H=16, L=32768, d=64, non-causal, scale 1/8, inputs
+Q, K, V ~ N(0,1) drawn by the seeded generator and rounded to bf16: the
+largest of the synthetic configurations, 4.4e12 FLOP per launch.  The inputs
+are resident in HBM when timing starts; L2 is flushed (a 512 MiB write)
+before every timed step, outside the timed events.
 
 FLOPs per step follow the metric: 4*B*H*L^2*d (halved when causal).
 ``value`` = whole-job TFLOP/s = N * FLOPs * K / max over ranks of the summed
@@ -17,23 +18,27 @@ host->device, runs the forward and copies O and LSE back, all inside the
 timed region; steps alternate two workspaces on two streams so one step's
 copies overlap the previous step (the serial figure is reported beside it).
 ``roofline`` compares the kernel against the measured dense bf16 peak.
-``cpu_baseline`` times the fp64 oracle on the host cores on the same inputs.
-``workloads`` lists the other synthetic configurations (device-generated
-seeded inputs), each timed the same way, including the d=128 non-causal
-L=8192 point used for the tensor-core fraction.  ``splitkv`` times the
-split-KV path (split pass + merge) against the single pass on shapes whose
-single-pass grid underfills the GPU.  ``backward`` times the backward pass
-(gradients by recomputation) on every workload: TFLOP/s by the convention
-10*B*H*L^2*d (five L x L x d products; halved when causal).  ``fp8`` times
-the FP8 forward (E4M3 Q and K with block scales, bf16 V) on every workload
-by the forward's convention, and the block quantisation of Q and K apart.
+``cpu_baseline`` times the fp64 oracle on the host cores on a bounded sample
+of the same inputs, after the GPU timing.
+``splitkv`` times the split-KV path (split pass + merge) against the single
+pass on shapes whose single-pass grid underfills the GPU.  ``backward`` times
+the backward pass (gradients by recomputation) on every workload: TFLOP/s by
+the convention 10*B*H*L^2*d (five L x L x d products; halved when causal).
+``fp8`` times the FP8 forward (E4M3 Q and K with block scales, bf16 V) on
+every workload by the forward's convention, against the dense FP8 ceiling
+(the measured bf16 peak times the nominal fp8/bf16 rate ratio of 2), and the
+block quantisation of Q and K apart.  ``workloads`` (the last key) lists the
+bf16 forward on every synthetic configuration (device-generated seeded
+inputs), each timed the same way, including the d=128 non-causal L=8192 point
+used for the tensor-core fraction.
 
 With more than one GPU (torchrun) every rank runs its own replica of the
 workload (the forward pass has no exchange step); only the timing is
 reduced (max over ranks).
 
 ``--impl reference`` times the fp64 CPU oracle instead (rank 0 only): each
-step is one oracle pass over a bounded sample of the headline workload.
+step is one oracle pass over a bounded sample of rows of the headline
+workload.
 """
 
 from __future__ import annotations
@@ -54,13 +59,17 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-HEADLINE = "B4_H8_L1024_d64"
+HEADLINE = "B1_H16_L32768_d64"
 METRIC = "attention fwd TFLOPS (4·B·H·L²·d) and % of GB300 dense BF16 tensor peak"
 FLUSH_BYTES = 512 << 20
 # NVIDIA's nominal dense bf16 tensor rate for one GB300, 2.25 PFLOP/s (its
 # published 2:4-sparse figure halved).  Reported as a second denominator next
 # to the measured peak; the roofline fractions use the measured one.
 NOMINAL_BF16_TFLOPS = 2250.0
+# Dense FP8 (E4M3) runs at twice the dense bf16 rate on this tensor core
+# (nominal 4.5 against 2.25 PFLOP/s); the FP8 ceiling is the measured bf16
+# peak scaled by that ratio.
+FP8_OVER_BF16 = 2.0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -194,9 +203,22 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------- CPU leg
-def oracle_sample_run(w, qb, kb, vb, heads, threads=0):
-    """One oracle pass over ``heads`` whole heads of the workload; returns
-    (seconds, flops)."""
+def row_flops(w, rows):
+    """Work of the given query rows of one head under the metric's convention:
+    4*L*d per row (non-causal); causal rows count their visible keys, 4*(i+1)*d
+    for row i (a whole head then sums to 2*L*(L+1)*d, the halved count up to
+    the diagonal)."""
+    import numpy as np
+    rows = np.asarray(rows, dtype=np.int64)
+    if w.causal:
+        return 4.0 * w.d * float((rows + 1).sum())
+    return 4.0 * w.L * w.d * rows.size
+
+
+def oracle_sample_run(w, qb, kb, vb, heads, n_rows, threads=0):
+    """One oracle pass over the first ``n_rows`` query rows of each of the
+    first ``heads`` heads of the workload (every key of those heads);
+    returns (seconds, flops)."""
     import numpy as np
 
     import oracle
@@ -205,29 +227,45 @@ def oracle_sample_run(w, qb, kb, vb, heads, threads=0):
     BH = w.B * w.H
     f = lambda b: bf16_bits_to_float32(b.reshape(BH, w.L, w.d)[:heads]).astype(np.float64)
     q, k, v = f(qb), f(kb), f(vb)
+    rows = None if n_rows >= w.L else [h * w.L + i for h in range(heads) for i in range(n_rows)]
     t0 = time.perf_counter()
-    oracle.attention(q, k, v, w.scale, w.causal, threads=threads)
+    oracle.attention(q, k, v, w.scale, w.causal, rows=rows, threads=threads)
     dt = time.perf_counter() - t0
-    return dt, w.flops * heads / BH
+    return dt, heads * row_flops(w, range(min(n_rows, w.L)))
 
 
-def cpu_baseline(w, qb, kb, vb, target_s=6.0):
+def sample_size(w, qb, kb, vb, target_s):
+    """(heads, rows per head) of a sample taking about ``target_s`` seconds:
+    rows of the first head while one head is more than enough, else whole
+    heads.  Sized from a probe of 256 rows."""
+    probe = min(256, w.L)
+    dt, _ = oracle_sample_run(w, qb, kb, vb, 1, probe)
+    per_row = max(dt, 1e-6) / probe
+    rows = int(target_s / per_row)
+    if rows < w.L:
+        return 1, max(1, rows)
+    return max(1, min(w.B * w.H, int(target_s / (per_row * w.L)))), w.L
+
+
+def cpu_baseline(w, qb, kb, vb, target_s=8.0):
     """Oracle TFLOP/s on the host cores, on a bounded sample of the workload."""
     BH = w.B * w.H
-    dt, fl = oracle_sample_run(w, qb, kb, vb, 1)
-    heads = max(1, min(BH, int(target_s / max(dt, 1e-3))))
-    reps = 1
-    if heads == BH:
-        dt, fl = oracle_sample_run(w, qb, kb, vb, BH)
-        reps = max(1, int(target_s / max(dt, 1e-3)))
-    total_t, total_f = 0.0, 0.0
-    for _ in range(reps):
-        dt, fl = oracle_sample_run(w, qb, kb, vb, heads)
-        total_t += dt
-        total_f += fl
+    heads, rows = sample_size(w, qb, kb, vb, target_s)
+    dt, fl = oracle_sample_run(w, qb, kb, vb, heads, rows)
     cores = os.cpu_count() or 1
-    return {"value": total_f / total_t / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"{heads} of {BH} heads of {w.name}, x{reps}, fp64, {total_t:.1f} s wall"}
+    what = (f"query rows 0..{rows - 1} of head 0" if heads == 1 and rows < w.L
+            else f"{heads} of {BH} whole heads")
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{what} of {w.name} (every key), fp64, {dt:.1f} s wall, "
+                      f"{cores} threads, after the GPU timing"}
+
+
+def step_stats(t):
+    """Mean, median, 90th percentile and minimum of per-step times (ms)."""
+    s = sorted(t)
+    p90 = s[min(len(s) - 1, int(math.ceil(0.9 * len(s))) - 1)]
+    return {"ms_mean": round(sum(s) / len(s), 5), "ms_median": round(statistics.median(s), 5),
+            "ms_p90": round(p90, 5), "ms_min": round(s[0], 5)}
 
 
 # ----------------------------------------------------------------- GPU leg
@@ -453,6 +491,15 @@ def whole_job_tflops(world, flops_per_step, steps, total_ms):
     return world * flops_per_step * steps / (total_ms * 1e-3) / 1e12
 
 
+def forward_line(w, t, peaks):
+    """Compact per-workload forward entry (kept short: the line's tail)."""
+    st = step_stats(t)
+    tf = w.flops / (st["ms_mean"] * 1e-3) / 1e12
+    return {"workload": w.name, "ms_mean": st["ms_mean"], "ms_median": st["ms_median"],
+            "tflops": round(tf, 1), "frac_of_peak": round(tf / peaks["bf16_tflops"], 4),
+            "steps": len(t)}
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -482,15 +529,11 @@ def run_ours(args):
         q, k, v = (x.to(dev) for x in host)
     flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
 
-    # CPU baseline first (before the GPU clocks are sampled), rank 0 only
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline and not args.device_inputs:
-        cpu = cpu_baseline(w, qb, kb, vb)
-
     extras = []
     splitkv = []
     backward = []
     fp8 = []
+    fp8_peak = FP8_OVER_BF16 * peaks["bf16_tflops"]
     with ClockSampler(local) as clk:
         if world > 1:
             dist.barrier()
@@ -504,29 +547,25 @@ def run_ours(args):
         if rank == 0 and not args.no_extra:
             for name, wx in WORKLOADS.items():
                 if name == w.name:
+                    extras.append(forward_line(wx, ms, peaks))
                     continue
                 qx, kx, vx = device_inputs(wx, dev, torch)
                 steps = max(3, min(args.extra_steps, int(2e13 / wx.flops)))
                 t = time_forward(fa, torch, qx, kx, vx, wx, steps, 3, flush_buf)
-                mean = sum(t) / len(t)
-                tf = wx.flops / (mean * 1e-3) / 1e12
-                extras.append({"workload": name, "B": wx.B, "H": wx.H, "L": wx.L, "d": wx.d,
-                               "causal": wx.causal, "ms_mean": round(mean, 4),
-                               "ms_min": round(min(t), 4), "tflops": round(tf, 1),
-                               "frac_of_peak": round(tf / peaks["bf16_tflops"], 4),
-                               "frac_of_nominal": round(tf / NOMINAL_BF16_TFLOPS, 4),
-                               "steps": steps})
+                extras.append(forward_line(wx, t, peaks))
                 del qx, kx, vx
             for name, wx in WORKLOADS.items():
                 steps = max(3, min(args.extra_steps, int(2e13 / wx.flops)))
                 tf8, tq = time_fp8(fa, torch, wx, dev, steps, 3, flush_buf)
                 m8, mq = sum(tf8) / len(tf8), sum(tq) / len(tq)
                 tr8, tr8_src = read_traffic(name, "fwd_fp8")
-                fp8.append({"workload": name, "ms_mean": round(m8, 4), "ms_min": round(min(tf8), 4),
+                t8 = wx.flops / (m8 * 1e-3) / 1e12
+                fp8.append({"workload": name, "ms_mean": round(m8, 4),
+                            "ms_min": round(min(tf8), 4),
                             "attention_kernel_dram_bytes": tr8, "traffic_source": tr8_src,
-                            "tflops": round(wx.flops / (m8 * 1e-3) / 1e12, 1),
-                            "frac_of_bf16_peak": round(wx.flops / (m8 * 1e-3) / 1e12
-                                                       / peaks["bf16_tflops"], 4),
+                            "tflops": round(t8, 1),
+                            "frac_of_fp8_peak": round(t8 / fp8_peak, 4),
+                            "frac_of_bf16_peak": round(t8 / peaks["bf16_tflops"], 4),
                             "quantize_qk_ms": round(mq, 4), "steps": steps})
             for name, wx in WORKLOADS.items():
                 steps = max(3, min(args.extra_steps,
@@ -553,12 +592,18 @@ def run_ours(args):
     if fa.fa_device_status(None, clear=True) != fa.FA_OK:
         raise RuntimeError("a kernel wait timed out during the benchmark")
 
+    # CPU baseline after the GPU timing (rank 0 only), so the timed region
+    # does not start on a GPU that sat idle for the seconds it takes
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline and not args.device_inputs:
+        cpu = cpu_baseline(w, qb, kb, vb)
+
     total_ms, total_e2e = max_over_ranks([sum(ms), sum(e2e_ms)], world, dist, dev)
     flops_step = w.flops
     value = whole_job_tflops(world, flops_step, args.steps, total_ms)
     e2e_value = whole_job_tflops(world, flops_step, args.steps, total_e2e)
-    mean_launch_ms = sum(ms) / len(ms)
-    achieved = flops_step / (mean_launch_ms * 1e-3) / 1e12
+    st = step_stats(ms)
+    achieved = flops_step / (st["ms_mean"] * 1e-3) / 1e12
     traffic, traffic_src = read_traffic(w.name)
 
     if rank == 0:
@@ -590,8 +635,7 @@ def run_ours(args):
                          "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed alone)",
                          "traffic": traffic, "traffic_source": traffic_src,
                          "algorithmic_bytes": w.algorithmic_bytes,
-                         "kernel": f"fa_fwd_kernel<{w.d},{str(w.causal).lower()}>",
-                         "ms_mean": round(mean_launch_ms, 5), "ms_min": round(min(ms), 5)},
+                         "kernel": f"fa_fwd_kernel<{w.d},{str(w.causal).lower()}>", **st},
             "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": round(total_e2e / args.steps, 5),
@@ -606,10 +650,14 @@ def run_ours(args):
             "gpu_launches": args.steps,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
-            "workloads": extras,
+            "fp8_peak": {"value": fp8_peak, "unit": "TFLOP/s",
+                         "source": f"{peak_src} bf16_tflops x {FP8_OVER_BF16} (nominal dense "
+                                   "fp8/bf16 rate ratio)"},
             "splitkv": splitkv,
-            "backward": backward,
             "fp8": fp8,
+            "backward": backward,
+            # last: the bf16 forward on every configuration (compact entries)
+            "workloads": extras,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -668,18 +716,19 @@ def run_reference(args):
     w = WORKLOADS[args.workload]
     qb, kb, vb = make_qkv(w)
     BH = w.B * w.H
-    # bounded sample per step: whole heads, about one second of host work
-    dt, _ = oracle_sample_run(w, qb, kb, vb, 1)
-    heads = max(1, min(BH, int(1.0 / max(dt, 1e-3))))
+    # bounded sample per step: about one second of host work
+    heads, rows = sample_size(w, qb, kb, vb, 1.0)
     for _ in range(args.warmup):
-        oracle_sample_run(w, qb, kb, vb, heads)
+        oracle_sample_run(w, qb, kb, vb, heads, rows)
     total_t, total_f = 0.0, 0.0
     for _ in range(args.steps):
-        t, f = oracle_sample_run(w, qb, kb, vb, heads)
+        t, f = oracle_sample_run(w, qb, kb, vb, heads, rows)
         total_t += t
         total_f += f
     value = total_f / total_t / 1e12
     cores = os.cpu_count() or 1
+    what = (f"query rows 0..{rows - 1} of head 0" if heads == 1 and rows < w.L
+            else f"{heads} of {BH} whole heads")
     line = {
         "impl": "reference",
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -690,7 +739,7 @@ def run_reference(args):
         "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d,
                    "causal": w.causal, "scale": w.scale},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{heads} of {BH} heads of {w.name} per step, fp64"},
+                         "sample": f"{what} of {w.name} per step (every key), fp64"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -217,10 +217,13 @@ constexpr int kMaxSplits = 64;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t{255}; }
 
+// Workspace of the split pass for the split count actually used
+// (split_plan's effective count, never more than the requested one).
 size_t workspace_bytes(int64_t BH, int L, int d, int n_splits) {
+  int ns = 1, bps = 1;
+  split_plan(L, n_splits, &ns, &bps);
   const size_t rows = static_cast<size_t>(BH) * static_cast<size_t>(L);
-  return align256(static_cast<size_t>(n_splits) * rows * d * 4) +
-         static_cast<size_t>(n_splits) * rows * 4;
+  return align256(static_cast<size_t>(ns) * rows * d * 4) + static_cast<size_t>(ns) * rows * 4;
 }
 
 // ---------------------------------------------------------------- backward
@@ -363,6 +366,7 @@ int fa_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o, 
                           fa_stream_t stream) {
   using namespace fa;
   if (n_splits < 1 || n_splits > kMaxSplits) return FA_ERR_INVALID_ARG;
+  // The scratch the call will use (for the effective split count) must fit.
   if (B >= 1 && H >= 1 && L >= 1 && (d == 64 || d == 128) &&
       workspace_bytes(static_cast<int64_t>(B) * H, L, d, n_splits) > FA_STATIC_WORKSPACE_BYTES)
     return FA_ERR_INVALID_ARG;  // the sizes need more scratch than the static array holds

@@ -30,8 +30,10 @@ rest.
 
 from __future__ import annotations
 
+import concurrent.futures
 import dataclasses
 import math
+import os
 
 import numpy as np
 
@@ -171,10 +173,25 @@ def bf16_bits_to_float32(b: np.ndarray) -> np.ndarray:
 
 
 def _fill(seed: int, start: int, n: int, std: float) -> np.ndarray:
+    """Counters ``[start, start + n)`` as bf16 bits.  Chunks are independent
+    (counter mode), so they are drawn on a thread pool: numpy releases the
+    interpreter lock inside its array operations, and every chunk's values
+    depend only on its counters, so the result is the same for any thread
+    count."""
     out = np.empty(n, dtype=np.uint16)
-    for lo in range(0, n, _CHUNK):
+
+    def chunk(lo):
         hi = min(n, lo + _CHUNK)
         out[lo:hi] = round_to_bf16_bits(std * normal_variates(seed, start + lo, hi - lo))
+
+    starts = range(0, n, _CHUNK)
+    workers = min(len(starts), os.cpu_count() or 1)
+    if workers <= 1:
+        for lo in starts:
+            chunk(lo)
+    else:
+        with concurrent.futures.ThreadPoolExecutor(max_workers=workers) as pool:
+            list(pool.map(chunk, starts))
     return out
 
 

@@ -109,10 +109,12 @@ int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *
 
 /*
  * fa_splitkv_workspace_bytes -- bytes of workspace fa_fwd_splitkv needs for
- * these sizes: 256-byte-aligned room for fp32 partial O [n_splits, B, H, L, d]
- * followed by fp32 partial LSE [n_splits, B, H, L].  Returns 0 for invalid
- * sizes (B/H/L < 1, d not 64/128, n_splits outside 1..64).  Host only; no
- * CUDA call.
+ * these sizes: 256-byte-aligned room for fp32 partial O [S, B, H, L, d]
+ * followed by fp32 partial LSE [S, B, H, L], where S is the split count the
+ * call actually uses: n_splits capped at the number of 128-key blocks
+ * ceil(L / 128), then reduced so that no split is left without a block.
+ * Returns 0 for invalid sizes (B/H/L < 1, d not 64/128, n_splits outside
+ * 1..64).  Host only; no CUDA call.
  */
 size_t fa_splitkv_workspace_bytes(int B, int H, int L, int d, int n_splits);
 
@@ -137,10 +139,14 @@ size_t fa_splitkv_workspace_bytes(int B, int H, int L, int d, int n_splits);
  * fa_splitkv_workspace_bytes(B, H, L, d, n_splits) exceeds
  * FA_STATIC_WORKSPACE_BYTES (fewer splits, or fa_fwd, then apply), and
  * otherwise the statuses of fa_fwd_splitkv.  The first call on a device looks
- * up the array's address on that device (with it current); make that first
- * call before any stream capture.  Every call uses the same array and finds
- * it as the previous call left it (nothing in it needs to start at zero), so
- * calls that overlap on the GPU race.
+ * up the array's address on that device (with it current) and keeps it for
+ * the life of the process; make that first call before any stream capture.
+ * The address belongs to the device's current context: after the context is
+ * destroyed (cudaDeviceReset) the kept address is stale, so do not call this
+ * entry point again in that process.  Every call uses the same array and
+ * finds it as the previous call left it (nothing in it needs to start at
+ * zero), so calls that overlap on the GPU -- on different streams, or from
+ * different host threads -- race.
  */
 int fa_fwd_splitkv_static(const void *q, const void *k, const void *v, void *o, float *lse,
                           int B, int H, int L, int d, float scale, int causal, int n_splits,

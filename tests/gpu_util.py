@@ -10,6 +10,19 @@ import numpy as np
 O_MAX_ABS = 1e-2
 O_MEAN_ABS = 1e-3
 LSE_MAX_ABS = 1e-3
+# Compute allowance of the per-element bound: the error the kernel may make
+# before its output is rounded to bf16.  It comes from rounding P~ to bf16
+# (relative error at most 2^-9 per weight) before the P~ V product, which
+# moves O_i by at most 2^-9 * sum_j (p_ij / l_i) |v_j|: 2^-9 for rows whose
+# probability-weighted mean |v| is at most 1 (V ~ N(0, 1) gives about 0.8;
+# a row dominated by one key carries that key's weight exactly, since the
+# running max makes it exp2(0) = 1).  fp32 accumulation adds ~1e-6.
+O_COMPUTE_ALLOW = 2.0 ** -9
+
+# (config, label, max|dO|, mean|dO - bf16(O_ref)|, mean|dO| vs exact, max|dLSE|)
+# of every check_parity call that names a configuration, printed as a table
+# at the end of the GPU session (tests/conftest.py).
+PARITY_LOG: list = []
 
 
 def bf16_ulp(x: np.ndarray) -> np.ndarray:
@@ -19,10 +32,10 @@ def bf16_ulp(x: np.ndarray) -> np.ndarray:
 
 
 def o_tolerance(o_ref: np.ndarray) -> np.ndarray:
-    """Per-element bound on |O_gpu - O_ref|: 1e-2, or one bf16 ulp of the exact
-    value where that ulp is larger (|O| >= 2): a bf16 output cannot be closer to
-    the exact value than faithful rounding."""
-    return np.maximum(O_MAX_ABS, bf16_ulp(o_ref))
+    """Per-element bound on |O_gpu - O_ref|: 1e-2, or, where it is larger,
+    half a bf16 ulp of the exact value (correct rounding of the output) plus
+    the compute allowance.  The second term passes 1e-2 only for |O| >= 4."""
+    return np.maximum(O_MAX_ABS, 0.5 * bf16_ulp(o_ref) + O_COMPUTE_ALLOW)
 
 
 def to_device(bits: np.ndarray, device):
@@ -40,14 +53,16 @@ def round_bf16(x: np.ndarray) -> np.ndarray:
     return bf16_bits_to_float32(round_to_bf16_bits(x)).astype(np.float64)
 
 
-def check_parity(o_gpu, lse_gpu, o_ref, lse_ref, label=""):
+def check_parity(o_gpu, lse_gpu, o_ref, lse_ref, label="", config=None):
     """Assert the tolerances; return (max|dO|, mean|dO| vs bf16(O_ref), max|dLSE|).
 
-    * every element: |O_gpu - O_ref| <= max(1e-2, bf16 ulp of O_ref);
+    * every element: |O_gpu - O_ref| <= max(1e-2, half a bf16 ulp of O_ref +
+      the compute allowance);
     * mean over elements: |O_gpu - bf16(O_ref)| <= 1e-3 -- the mean error of
       the computation, measured against the exact result in the output's own
       format (rounding the exact O to bf16 alone costs up to ~8.5e-4 in mean
-      when |O| ~ 1, which would otherwise eat the whole budget);
+      when |O| ~ 1, which would otherwise eat the whole budget); the mean
+      against the unrounded O_ref is logged beside it (``config``);
     * LSE (fp32 output): |LSE_gpu - LSE_ref| <= 1e-3 everywhere.
     """
     err = np.abs(o_gpu - o_ref)
@@ -58,9 +73,11 @@ def check_parity(o_gpu, lse_gpu, o_ref, lse_ref, label=""):
     mean_err = float(np.abs(o_gpu - round_bf16(o_ref)).mean())
     assert mean_err <= O_MEAN_ABS, (f"{label}: mean |O - bf16(O_ref)| {mean_err:.3e} "
                                     f"(vs unrounded {err.mean():.3e})")
-    el = np.abs(lse_gpu - lse_ref).max()
+    el = float(np.abs(lse_gpu - lse_ref).max())
     assert el <= LSE_MAX_ABS, f"{label}: max |dLSE| {el:.3e}"
-    return float(err.max()), mean_err, float(el)
+    if config is not None:
+        PARITY_LOG.append((config, label, float(err.max()), mean_err, float(err.mean()), el))
+    return float(err.max()), mean_err, el
 
 
 # Gradients (backward pass).  Per head and per gradient tensor G, against the

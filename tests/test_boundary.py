@@ -118,9 +118,13 @@ def test_product_path_does_not_import_the_oracle():
 def test_splitkv_workspace_bytes(lib):
     B, H, L, d, S = 2, 3, 300, 64, 5
     rows = B * H * L
-    o_bytes = S * rows * d * 4
-    expect = ((o_bytes + 255) // 256) * 256 + S * rows * 4
+    used = 3  # five splits asked for over ceil(300 / 128) = 3 key blocks
+    o_bytes = used * rows * d * 4
+    expect = ((o_bytes + 255) // 256) * 256 + used * rows * 4
     assert fa.fa_splitkv_workspace_bytes(B, H, L, d, S) == expect
+    S2, L2 = 2, 1000  # two splits over 8 blocks: both used
+    expect2 = ((S2 * B * H * L2 * d * 4 + 255) // 256) * 256 + S2 * B * H * L2 * 4
+    assert fa.fa_splitkv_workspace_bytes(B, H, L2, d, S2) == expect2
     assert fa.fa_splitkv_workspace_bytes(B, H, L, 96, S) == 0
     assert fa.fa_splitkv_workspace_bytes(B, H, L, d, 0) == 0
     assert fa.fa_splitkv_workspace_bytes(B, H, L, d, 65) == 0

@@ -76,21 +76,43 @@ def test_quantisation_edge_values(dev):
     assert np.array_equal(codes.reshape(1, L, d), ref_codes)
 
 
-def _fp8_case(dev, qb, kb, vb, scale, causal, label):
+def _host_quantised(bits, BH, L, d):
+    """The oracle's E4M3 codes and block scales of a bf16 input, quantised on
+    the host from the input itself (never from the GPU's codes)."""
+    return ofp8.quantize_blocks(_f32(bits).reshape(BH, L, d))
+
+
+def _assert_same_codes(dev_codes, dev_scales, ref_codes, ref_scales, label):
+    got_c = dev_codes.cpu().numpy().reshape(ref_codes.shape)
+    got_s = dev_scales.cpu().numpy().reshape(ref_scales.shape).astype(np.float32)
+    assert np.array_equal(got_s.view(np.uint32), ref_scales.astype(np.float32).view(np.uint32)), \
+        f"{label}: block scales differ from the oracle's"
+    bad = got_c != ref_codes
+    assert not bad.any(), f"{label}: {int(bad.sum())} E4M3 codes differ from the oracle's"
+
+
+def _fp8_case(dev, qb, kb, vb, scale, causal, label, config=None):
     import torch
     B, H, L, d = qb.shape
+    BH = B * H
     q, k, v = (to_device(x, dev) for x in (qb, kb, vb))
     q8, qs = fa.quantize_fp8(q)
     k8, ks = fa.quantize_fp8(k)
     o, lse = fa.forward_fp8(q8, k8, v, qs, ks, scale=scale, causal=causal)
     torch.cuda.synchronize()
-    qd = ofp8.dequantize_blocks(q8.cpu().numpy().reshape(B * H, L, d), qs.cpu().numpy().reshape(B * H, -1))
-    kd = ofp8.dequantize_blocks(k8.cpu().numpy().reshape(B * H, L, d), ks.cpu().numpy().reshape(B * H, -1))
-    vd = _f32(vb).astype(np.float64).reshape(B * H, L, d)
+    # expected result: exact attention of the oracle's own quantisation of
+    # the host inputs; the GPU's codes must equal those bit for bit
+    qc, qsc = _host_quantised(qb, BH, L, d)
+    kc, ksc = _host_quantised(kb, BH, L, d)
+    _assert_same_codes(q8, qs, qc, qsc, label + " Q")
+    _assert_same_codes(k8, ks, kc, ksc, label + " K")
+    qd = ofp8.dequantize_blocks(qc, qsc)
+    kd = ofp8.dequantize_blocks(kc, ksc)
+    vd = _f32(vb).astype(np.float64).reshape(BH, L, d)
     o_ref, lse_ref = oracle.attention(qd, kd, vd, scale, causal)
-    return check_parity(from_device(o).reshape(B * H, L, d),
-                        lse.cpu().numpy().astype(np.float64).reshape(B * H, L),
-                        o_ref, lse_ref, label)
+    return check_parity(from_device(o).reshape(BH, L, d),
+                        lse.cpu().numpy().astype(np.float64).reshape(BH, L),
+                        o_ref, lse_ref, label, config)
 
 
 @pytest.mark.parametrize("L", [1, 17, 128, 129, 300, 1000])
@@ -112,7 +134,7 @@ def test_fp8_forward_batch_heads_and_scales(dev, d):
 def test_fp8_forward_benchmark_workload(dev):
     w = WORKLOADS["B4_H8_L1024_d64"]
     qb, kb, vb = make_qkv(w)
-    _fp8_case(dev, qb, kb, vb, w.scale, w.causal, "fp8 " + w.name)
+    _fp8_case(dev, qb, kb, vb, w.scale, w.causal, "fp8 " + w.name, config="fp8 " + w.name)
 
 
 @pytest.mark.parametrize("name", ["gate_B1_H32_L8192_d128", "B1_H32_L16384_d128_causal_qk3"])
@@ -128,12 +150,19 @@ def test_fp8_forward_full_size_sampled(dev, name):
     torch.cuda.synchronize()
     rng = np.random.default_rng(w.seed)
     rows = sorted({0, 1, 127, 128, w.L // 2, w.L - 1} | set(int(x) for x in rng.integers(0, w.L, 8)))
-    vf = vb.reshape(BH, w.L, w.d)
+    qf, kf, vf = (x.reshape(BH, w.L, w.d) for x in (qb, kb, vb))
     for h in (0, BH - 1):
-        qd = ofp8.dequantize_blocks(q8[0, h].cpu().numpy()[None], qs[0, h].cpu().numpy()[None])[0]
-        kd = ofp8.dequantize_blocks(k8[0, h].cpu().numpy()[None], ks[0, h].cpu().numpy()[None])[0]
+        # the oracle quantises this head's Q and K from the host inputs
+        qc, qsc = _host_quantised(qf[h], 1, w.L, w.d)
+        kc, ksc = _host_quantised(kf[h], 1, w.L, w.d)
+        _assert_same_codes(q8.view(BH, w.L, w.d)[h], qs.view(BH, -1)[h], qc, qsc,
+                           f"fp8 {name} head {h} Q")
+        _assert_same_codes(k8.view(BH, w.L, w.d)[h], ks.view(BH, -1)[h], kc, ksc,
+                           f"fp8 {name} head {h} K")
+        qd = ofp8.dequantize_blocks(qc, qsc)[0]
+        kd = ofp8.dequantize_blocks(kc, ksc)[0]
         o_ref, lse_ref = oracle.attention(qd, kd, _f32(vf[h]).astype(np.float64), w.scale,
                                           w.causal, rows=rows)
         check_parity(from_device(o.view(BH, w.L, w.d)[h, rows]),
                      lse.view(BH, w.L)[h, rows].cpu().numpy().astype(np.float64), o_ref, lse_ref,
-                     f"fp8 {name} head {h}")
+                     f"fp8 {name} head {h}", config="fp8 " + name)

@@ -5,10 +5,10 @@ inference engine or plugin host that owns the whole memory budget and gives
 out no scratch.  For them the library keeps its own split-KV scratch array
 (FA_STATIC_WORKSPACE_BYTES, in device global memory) and this entry point
 takes no workspace.  The tests call it through the C ABI and compare it with
-fa_fwd_splitkv, which uses a caller-provided workspace, on the same inputs,
-on two calls in a row: the second call finds the array as the first one left
-it.  This file is collected last so that a run stopping at the first failure
-has already run every other test.
+the fp64 oracle and with fa_fwd_splitkv (which uses a caller-provided
+workspace) on the same inputs, on two calls in a row: the second call finds
+the array as the first one left it.  This file is collected last so that a
+run stopping at the first failure has already run every other test.
 """
 
 from __future__ import annotations
@@ -17,8 +17,10 @@ import numpy as np
 import pytest
 
 import exact_tiled_attention_09_gb300 as fa
-from fa_inputs import make_custom
-from tests.gpu_util import LSE_MAX_ABS, O_MEAN_ABS, from_device, o_tolerance, to_device
+import oracle
+from fa_inputs import bf16_bits_to_float32, make_custom
+from tests.gpu_util import (LSE_MAX_ABS, O_MEAN_ABS, check_parity, from_device, o_tolerance,
+                            to_device)
 
 
 def test_static_entry_rejects_sizes_beyond_its_array():
@@ -32,6 +34,18 @@ def test_static_entry_rejects_sizes_beyond_its_array():
                                     64, 0.1, 0, 0, None) == fa.FA_ERR_INVALID_ARG
 
 
+def test_scratch_size_follows_the_splits_actually_used():
+    # 64 splits requested over 8 key blocks: 8 are used, and the size (which
+    # the static entry point checks against its array) is that of 8
+    B, H, L, d = 1, 2, 1000, 128
+    assert fa.fa_splitkv_workspace_bytes(B, H, L, d, 64) == fa.fa_splitkv_workspace_bytes(
+        B, H, L, d, 8)
+    assert fa.fa_splitkv_workspace_bytes(B, H, L, d, 64) <= fa.FA_STATIC_WORKSPACE_BYTES
+    # 7 splits over 8 blocks take 2 blocks each: 4 splits
+    assert fa.fa_splitkv_workspace_bytes(B, H, L, d, 7) == fa.fa_splitkv_workspace_bytes(
+        B, H, L, d, 4)
+
+
 @pytest.mark.gpu
 def test_static_entry_matches_workspace_entry_on_two_calls():
     torch = pytest.importorskip("torch")
@@ -42,13 +56,15 @@ def test_static_entry_matches_workspace_entry_on_two_calls():
     cases = [  # (B, H, L, d, causal, n_splits, seed): larger first, then smaller
         (1, 2, 1000, 128, 1, 4, 11),
         (2, 3, 700, 64, 0, 3, 12),
+        # 64 splits asked for over 8 key blocks: 8 used (64 would not fit)
+        (1, 2, 1000, 128, 0, 64, 13),
     ]
     for B, H, L, d, causal, S, seed in cases:
         assert fa.fa_splitkv_workspace_bytes(B, H, L, d, S) <= fa.FA_STATIC_WORKSPACE_BYTES
         qb, kb, vb = make_custom(B, H, L, d, seed=seed)
         q, k, v = (to_device(x, dev) for x in (qb, kb, vb))
         scale = 1.0 / np.sqrt(d)
-        o_ref, lse_ref = fa.forward_splitkv(q, k, v, S, scale=scale, causal=bool(causal))
+        o_ws, lse_ws = fa.forward_splitkv(q, k, v, S, scale=scale, causal=bool(causal))
         o = torch.full_like(q, float("nan"))
         lse = torch.full((B, H, L), float("nan"), device=dev)
         stream = torch.cuda.current_stream(dev)
@@ -57,10 +73,16 @@ def test_static_entry_matches_workspace_entry_on_two_calls():
                                       stream.cuda_stream)
         assert rc == fa.FA_OK, fa.fa_status_string(rc)
         torch.cuda.synchronize()
-        a, b = from_device(o), from_device(o_ref)
+        a, b = from_device(o), from_device(o_ws)
         assert np.isfinite(a).all()
+        # against the entry point with a caller workspace
         err = np.abs(a - b)
         assert (err <= o_tolerance(b)).all() and err.mean() <= O_MEAN_ABS
-        dl = (lse - lse_ref).abs().max().item()
+        dl = (lse - lse_ws).abs().max().item()
         assert dl <= LSE_MAX_ABS
+        # against the fp64 oracle on the same inputs
+        f = lambda x: bf16_bits_to_float32(x).astype(np.float64)
+        o_ref, lse_ref = oracle.attention(f(qb), f(kb), f(vb), scale, bool(causal))
+        check_parity(a, lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
+                     f"static split-KV B={B} H={H} L={L} d={d} causal={causal} S={S}")
     assert fa.fa_device_status(None, clear=True) == fa.FA_OK
