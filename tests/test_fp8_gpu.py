@@ -18,7 +18,7 @@ import exact_tiled_attention_09_gb300 as fa
 import oracle
 from oracle import fp8 as ofp8
 from fa_inputs import WORKLOADS, bf16_bits_to_float32, make_custom, make_qkv, round_to_bf16_bits
-from tests.gpu_util import check_parity, from_device, to_device
+from tests.gpu_util import check_parity, oracle_forward, from_device, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -109,10 +109,10 @@ def _fp8_case(dev, qb, kb, vb, scale, causal, label, config=None):
     qd = ofp8.dequantize_blocks(qc, qsc)
     kd = ofp8.dequantize_blocks(kc, ksc)
     vd = _f32(vb).astype(np.float64).reshape(BH, L, d)
-    o_ref, lse_ref = oracle.attention(qd, kd, vd, scale, causal)
+    o_ref, lse_ref, a_ref = oracle_forward(qd, kd, vd, scale, causal)
     return check_parity(from_device(o).reshape(BH, L, d),
                         lse.cpu().numpy().astype(np.float64).reshape(BH, L),
-                        o_ref, lse_ref, label, config)
+                        o_ref, lse_ref, label, config, absv_ref=a_ref)
 
 
 @pytest.mark.parametrize("L", [1, 17, 128, 129, 300, 1000])
@@ -161,8 +161,8 @@ def test_fp8_forward_full_size_sampled(dev, name):
                            f"fp8 {name} head {h} K")
         qd = ofp8.dequantize_blocks(qc, qsc)[0]
         kd = ofp8.dequantize_blocks(kc, ksc)[0]
-        o_ref, lse_ref = oracle.attention(qd, kd, _f32(vf[h]).astype(np.float64), w.scale,
+        o_ref, lse_ref, a_ref = oracle_forward(qd, kd, _f32(vf[h]).astype(np.float64), w.scale,
                                           w.causal, rows=rows)
         check_parity(from_device(o.view(BH, w.L, w.d)[h, rows]),
                      lse.view(BH, w.L)[h, rows].cpu().numpy().astype(np.float64), o_ref, lse_ref,
-                     f"fp8 {name} head {h}", config="fp8 " + name)
+                     f"fp8 {name} head {h}", config="fp8 " + name, absv_ref=a_ref)

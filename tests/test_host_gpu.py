@@ -13,9 +13,8 @@ import numpy as np
 import pytest
 
 import exact_tiled_attention_09_gb300 as fa
-import oracle
 from fa_inputs import bf16_bits_to_float32, make_custom
-from tests.gpu_util import check_parity, to_device
+from tests.gpu_util import check_parity, oracle_forward, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -60,9 +59,9 @@ def test_host_forward_equals_device_forward(dev, packed, d, causal):
     assert bool((o.view(torch.int16) == od.cpu().view(torch.int16)).all())
     assert bool((lse == ld.cpu()).all())
     f = lambda b: bf16_bits_to_float32(b).astype(np.float64)
-    o_ref, lse_ref = oracle.attention(f(qb), f(kb), f(vb), 0.1, causal)
+    o_ref, lse_ref, a_ref = oracle_forward(f(qb), f(kb), f(vb), 0.1, causal)
     check_parity(o.float().numpy().astype(np.float64), lse.numpy().astype(np.float64), o_ref,
-                 lse_ref, f"host packed={packed}")
+                 lse_ref, f"host packed={packed}", absv_ref=a_ref)
 
 
 def test_host_forward_pipelined_on_two_streams(dev):

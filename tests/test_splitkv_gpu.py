@@ -13,9 +13,8 @@ import numpy as np
 import pytest
 
 import exact_tiled_attention_09_gb300 as fa
-import oracle
 from fa_inputs import bf16_bits_to_float32, make_custom
-from tests.gpu_util import check_parity, from_device, to_device
+from tests.gpu_util import check_parity, oracle_forward, from_device, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -52,9 +51,9 @@ def test_splitkv_parity(dev, n_splits, L, d, causal):
     qb, kb, vb = make_custom(1, 2, L, d, seed=3000 + L + d + n_splits + int(causal))
     scale = 1.0 / math.sqrt(d)
     o, lse = _split(dev, qb, kb, vb, scale, causal, n_splits)
-    o_ref, lse_ref = oracle.attention(_f64(qb), _f64(kb), _f64(vb), scale, causal)
+    o_ref, lse_ref, a_ref = oracle_forward(_f64(qb), _f64(kb), _f64(vb), scale, causal)
     check_parity(from_device(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
-                 f"split={n_splits} L={L} d={d} causal={causal}")
+                 f"split={n_splits} L={L} d={d} causal={causal}", absv_ref=a_ref)
 
 
 @pytest.mark.parametrize("L", [1, 2, 127])
@@ -62,9 +61,9 @@ def test_splitkv_short_sequences(dev, L):
     # more splits requested than key blocks: the pass uses one split
     qb, kb, vb = make_custom(2, 3, L, 64, seed=77 + L)
     o, lse = _split(dev, qb, kb, vb, 0.125, True, 8)
-    o_ref, lse_ref = oracle.attention(_f64(qb), _f64(kb), _f64(vb), 0.125, True)
+    o_ref, lse_ref, a_ref = oracle_forward(_f64(qb), _f64(kb), _f64(vb), 0.125, True)
     check_parity(from_device(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
-                 f"short L={L}")
+                 f"short L={L}", absv_ref=a_ref)
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -77,9 +76,9 @@ def test_splitkv_long_sequence_sampled(dev, causal):
     rows = np.array([0, 1, 127, 128, 255, 256, 4095, 4096, 8190, 8191])
     for h in (0, 3):
         qh, kh, vh = (_f64(x[0, h]) for x in (qb, kb, vb))
-        o_ref, lse_ref = oracle.attention(qh, kh, vh, 1.0 / math.sqrt(d), causal, rows=rows)
+        o_ref, lse_ref, a_ref = oracle_forward(qh, kh, vh, 1.0 / math.sqrt(d), causal, rows=rows)
         check_parity(from_device(o[0, h, rows]), lse[0, h, rows].cpu().numpy().astype(np.float64),
-                     o_ref, lse_ref, f"L=8192 head {h} causal={causal}")
+                     o_ref, lse_ref, f"L=8192 head {h} causal={causal}", absv_ref=a_ref)
 
 
 def test_splitkv_matches_single_pass(dev):
@@ -100,6 +99,6 @@ def test_splitkv_workspace_reuse(dev):
     for seed in (1, 2):
         qb, kb, vb = make_custom(1, 2, L, d, seed=seed)
         o, lse = _split(dev, qb, kb, vb, 0.1, bool(seed % 2), S, workspace=ws)
-        o_ref, lse_ref = oracle.attention(_f64(qb), _f64(kb), _f64(vb), 0.1, bool(seed % 2))
+        o_ref, lse_ref, a_ref = oracle_forward(_f64(qb), _f64(kb), _f64(vb), 0.1, bool(seed % 2))
         check_parity(from_device(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
-                     f"reuse seed {seed}")
+                     f"reuse seed {seed}", absv_ref=a_ref)

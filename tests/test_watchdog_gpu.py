@@ -21,7 +21,7 @@ import pytest
 import exact_tiled_attention_09_gb300 as fa
 import oracle
 from fa_inputs import bf16_bits_to_float32, make_custom
-from tests.gpu_util import check_parity, from_device, to_device
+from tests.gpu_util import check_parity, oracle_forward, from_device, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -76,9 +76,9 @@ def test_wait_that_runs_out_is_reported_and_the_context_survives(dev, d, causal,
     o, lse = run()
     torch.cuda.synchronize()
     assert fa.fa_device_status(None, clear=True) == fa.FA_OK
-    o_ref, lse_ref = oracle.attention(_f64(qb), _f64(kb), _f64(vb), scale, causal)
+    o_ref, lse_ref, a_ref = oracle_forward(_f64(qb), _f64(kb), _f64(vb), scale, causal)
     check_parity(from_device(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
-                 f"after timeout d={d} causal={causal} split={split}")
+                 f"after timeout d={d} causal={causal} split={split}", absv_ref=a_ref)
 
 
 @pytest.mark.parametrize("d,causal", [(64, False), (128, True)])

@@ -17,10 +17,8 @@ import numpy as np
 import pytest
 
 import exact_tiled_attention_09_gb300 as fa
-import oracle
 from fa_inputs import bf16_bits_to_float32, make_custom
-from tests.gpu_util import (LSE_MAX_ABS, O_MEAN_ABS, check_parity, from_device, o_tolerance,
-                            to_device)
+from tests.gpu_util import check_parity, from_device, oracle_forward, to_device
 
 
 def test_static_entry_rejects_sizes_beyond_its_array():
@@ -73,16 +71,15 @@ def test_static_entry_matches_workspace_entry_on_two_calls():
                                       stream.cuda_stream)
         assert rc == fa.FA_OK, fa.fa_status_string(rc)
         torch.cuda.synchronize()
-        a, b = from_device(o), from_device(o_ws)
+        a = from_device(o)
         assert np.isfinite(a).all()
-        # against the entry point with a caller workspace
-        err = np.abs(a - b)
-        assert (err <= o_tolerance(b)).all() and err.mean() <= O_MEAN_ABS
-        dl = (lse - lse_ws).abs().max().item()
-        assert dl <= LSE_MAX_ABS
+        # against the entry point with a caller workspace: the same kernels on
+        # the same inputs, only the scratch differs, so the bits agree
+        assert bool((o.view(torch.int16) == o_ws.view(torch.int16)).all())
+        assert bool((lse == lse_ws).all())
         # against the fp64 oracle on the same inputs
         f = lambda x: bf16_bits_to_float32(x).astype(np.float64)
-        o_ref, lse_ref = oracle.attention(f(qb), f(kb), f(vb), scale, bool(causal))
+        o_ref, lse_ref, a_ref = oracle_forward(f(qb), f(kb), f(vb), scale, bool(causal))
         check_parity(a, lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
-                     f"static split-KV B={B} H={H} L={L} d={d} causal={causal} S={S}")
+                     f"static split-KV B={B} H={H} L={L} d={d} causal={causal} S={S}", absv_ref=a_ref)
     assert fa.fa_device_status(None, clear=True) == fa.FA_OK
