@@ -126,7 +126,7 @@ struct FwdCfg {
   // q_full, full[NSLOT], empty[NSLOT], s_full[2], p_full[2], o_done[2],
   // drain[2] (one per MMA warp), s_free[2], xchg[2][4] (split rows: one
   // per tile and quarter, the two column halves' warps arrive)
-  static constexpr int NBAR = 1 + 2 * NSLOT + 2 + 2 + 2 + 2 + 2 + 8;
+  static constexpr int NBAR = 1 + 2 * NSLOT + 2 + 2 + 2 + 2 + 2 + (COL_SPLIT == 2 ? 8 : 0);
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   // Split rows: partial row maxima (and at the end partial row sums), fp32
   // [tile][block parity][column half][row]
@@ -272,7 +272,8 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
     for (int t = 0; t < TILES_PER_CTA; ++t) {
       mbar_init(bar_drain(t), 1);
       mbar_init(bar_sfree(t), C::WARPS_PER_TILE);  // one arrival per softmax warp
-      for (int qr = 0; qr < 4; ++qr) mbar_init(bar_xchg(t, qr), 2);  // both column halves
+      if constexpr (C::COL_SPLIT == 2)
+        for (int qr = 0; qr < 4; ++qr) mbar_init(bar_xchg(t, qr), 2);  // both column halves
     }
     *abort_flag = 0;
     fence_mbarrier_init();
@@ -535,8 +536,8 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
     constexpr int NCH = C::KEYS_PER_WARP / 32;        // 32-column score chunks
     constexpr int OCH = D / 32 / C::COL_SPLIT;        // 32-column O chunks
     const int sidx = warp - FIRST_SOFTMAX_WARP;
-    const int t = sidx / C::WARPS_PER_TILE;           // Q tile of this warp
-    const int half = (sidx >> 2) % C::COL_SPLIT;      // key-column half (split rows)
+    const int t = (sidx >> 2) >> (C::COL_SPLIT - 1);  // Q tile of this warp
+    const int half = (sidx >> 2) & (C::COL_SPLIT - 1);  // key-column half (split rows)
     const int quarter = warp & 3;     // TMEM lanes this warp may access
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
