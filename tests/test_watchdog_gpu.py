@@ -81,6 +81,38 @@ def test_wait_that_runs_out_is_reported_and_the_context_survives(dev, d, causal,
                  f"after timeout d={d} causal={causal} split={split}", absv_ref=a_ref)
 
 
+@pytest.mark.parametrize("d,causal", [(64, False), (64, True), (128, False)])
+def test_fp8_wait_that_runs_out_is_reported(dev, d, causal):
+    # FP8 at d = 64 runs its own warp layout (two softmax warps per row, an
+    # MMA warp per tile): every role must still stop, drain and return
+    import torch
+    from tests.test_fp8_gpu import _fp8_case
+    B, H, L = 2, 3, 600
+    qb, kb, vb = make_custom(B, H, L, d, seed=720 + d + int(causal))
+    q, k, v = (to_device(x, dev) for x in (qb, kb, vb))
+    scale = 1.0 / math.sqrt(d)
+    q8, qs = fa.quantize_fp8(q)
+    k8, ks = fa.quantize_fp8(k)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status(None, clear=True) == fa.FA_OK
+    try:
+        fa.fa_set_wait_timeout_ns(SHORT_LIMIT_NS)
+        fa.fa_test_withhold_q_load(True)
+        t0 = time.time()
+        fa.forward_fp8(q8, k8, v, qs, ks, scale=scale, causal=causal)
+        torch.cuda.synchronize()
+        elapsed = time.time() - t0
+        status = fa.fa_device_status(None, clear=True)
+    finally:
+        fa.fa_test_withhold_q_load(False)
+        fa.fa_set_wait_timeout_ns(DEFAULT_LIMIT_NS)
+    assert status == fa.FA_ERR_TIMEOUT
+    assert elapsed < 10.0, f"the withheld wait took {elapsed:.1f} s to end"
+    # the same context keeps working: a full FP8 forward against the oracle
+    _fp8_case(dev, qb, kb, vb, scale, causal, f"fp8 after timeout d={d} causal={causal}")
+    assert fa.fa_device_status(None, clear=True) == fa.FA_OK
+
+
 @pytest.mark.parametrize("d,causal", [(64, False), (128, True)])
 def test_backward_wait_that_runs_out_is_reported(dev, d, causal):
     import torch
