@@ -203,17 +203,22 @@ def test_outputs_fully_overwritten(dev):
     assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(lse).all())
 
 
-def test_no_write_past_the_outputs(dev):
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("L", [129, 300])
+def test_no_write_past_the_outputs(dev, d, causal, L):
+    # O leaves through a tile-sized store whose rows past L are clipped by
+    # the tensor map: nothing may land past the caller's buffer
     import torch
-    L, d = 129, 64
-    qb, kb, vb = make_custom(1, 1, L, d, seed=66)
+    qb, kb, vb = make_custom(1, 1, L, d, seed=66 + L + d)
     q, k, v = (to_device(x, dev) for x in (qb, kb, vb))
     o_big = torch.full((L + 256, d), 7.0, dtype=torch.bfloat16, device=dev)
     lse_big = torch.full((L + 256,), 7.0, device=dev)
-    fa.forward(q, k, v, scale=0.125, causal=False, out=o_big[:L].view(1, 1, L, d),
+    fa.forward(q, k, v, scale=0.125, causal=causal, out=o_big[:L].view(1, 1, L, d),
                lse=lse_big[:L].view(1, 1, L))
     torch.cuda.synchronize()
     assert bool((o_big[L:] == 7.0).all()) and bool((lse_big[L:] == 7.0).all())
+    assert bool(torch.isfinite(o_big[:L]).all())
 
 
 def test_status_after_runs_is_ok(dev):
