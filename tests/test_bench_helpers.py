@@ -45,3 +45,23 @@ def test_committed_summaries_carry_the_lookup_fields():
             assert traffic == float(fields["dram_bytes_per_launch"].group(1)) and src
         else:
             assert traffic is None or src != os.path.relpath(path, bench.ROOT)
+
+
+def test_step_stats():
+    st = bench.step_stats([3.0, 1.0, 2.0, 10.0, 4.0, 5.0, 6.0, 7.0, 8.0, 9.0])
+    assert st["ms_mean"] == 5.5 and st["ms_median"] == 5.5 and st["ms_min"] == 1.0
+    assert st["ms_p90"] == 9.0  # the 9th of 10 sorted values
+    one = bench.step_stats([2.5])
+    assert one["ms_mean"] == one["ms_median"] == one["ms_p90"] == one["ms_min"] == 2.5
+
+
+def test_row_flops_follow_the_metric():
+    from fa_inputs import AttentionWorkload
+    w = AttentionWorkload("t", 1, 1, 100, 64, False, 0.125, 1)
+    assert bench.row_flops(w, range(100)) == w.flops          # a whole head, non-causal
+    assert bench.row_flops(w, [0, 5]) == 2 * 4 * 100 * 64
+    wc = AttentionWorkload("t", 1, 1, 100, 64, True, 0.125, 1)
+    # causal: row i sees i + 1 keys; a whole head is 2 L (L + 1) d, the
+    # metric's halved count up to the diagonal
+    assert bench.row_flops(wc, range(100)) == 2 * 100 * 101 * 64
+    assert abs(bench.row_flops(wc, range(100)) / wc.flops - 1) < 0.011
