@@ -223,3 +223,32 @@ def test_no_write_past_the_outputs(dev, d, causal, L):
 
 def test_status_after_runs_is_ok(dev):
     assert fa.fa_device_status(None, clear=False) == fa.FA_OK
+
+
+# ------------------------------------------------------------------ scheduling
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_many_heads_in_several_scheduling_groups(dev, d, causal):
+    # 960 heads of L = 256: heads are scheduled in groups whose K and V fit
+    # in ~32 MB of L2 (512 heads a group at d = 64, 256 at d = 128), so
+    # this covers several groups, a ragged last group and, causal, the
+    # longest-first order across the heads of a group; every head in full
+    B, H, L = 15, 64, 256
+    qb, kb, vb = make_custom(B, H, L, d, seed=1300 + d + int(causal))
+    _full_parity(dev, qb, kb, vb, 1.0 / math.sqrt(d), causal,
+                 f"B={B} H={H} L={L} d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("L,d,causal", [(65536, 64, False), (40000, 128, True)])
+def test_one_very_long_head_sampled(dev, L, d, causal):
+    # one head, far longer than the workloads: 256-512 key blocks per CTA
+    import torch
+    qb, kb, vb = make_custom(1, 1, L, d, seed=1400 + d)
+    o, lse = _run(dev, qb, kb, vb, 1.0 / math.sqrt(d), causal)
+    rng = np.random.default_rng(L)
+    rows = _sample_rows(L, rng, n_random=10)
+    f = lambda x: _f64(x.reshape(L, d))
+    o_ref, lse_ref, a_ref = oracle_forward(f(qb), f(kb), f(vb), 1.0 / math.sqrt(d), causal,
+                                           rows=rows)
+    check_parity(from_device(o.view(L, d)[rows]), lse.view(L)[rows].cpu().numpy().astype(np.float64),
+                 o_ref, lse_ref, f"L={L} d={d} causal={causal}", absv_ref=a_ref)
