@@ -69,6 +69,21 @@ def test_bwd_ragged_lengths(dev, L, d, causal):
                  f"L={L} d={d} causal={causal}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_many_heads_in_several_scheduling_groups(dev, d, causal):
+    # 600 heads of L = 256: the backward schedules heads in groups whose Q,
+    # dO and dQ accumulator fit in ~32 MB of L2 (256 heads a group at
+    # d = 64, 128 at d = 128): several groups, a ragged last group and,
+    # causal, the longest-first order; every head in full
+    B, H, L = 10, 60, 256
+    seed = 3500 + d + int(causal)
+    qb, kb, vb = make_custom(B, H, L, d, seed)
+    dob = make_custom_grad_out(B, H, L, d, seed)
+    _full_parity(dev, qb, kb, vb, dob, 1.0 / math.sqrt(d), causal,
+                 f"B={B} H={H} L={L} d={d} causal={causal}")
+
+
 @pytest.mark.parametrize("B,H", [(2, 3), (3, 1)])
 @pytest.mark.parametrize("d", [64, 128])
 def test_bwd_batch_heads(dev, B, H, d):
