@@ -646,7 +646,10 @@ def run_ours(args):
                     "serial_value": round(world * flops_step * len(e2e_serial)
                                           / (sum(e2e_serial) * 1e-3) / 1e12, 3),
                     "l2": "inputs are re-copied from the host every step (no flush "
-                          "in the pipelined run; the serial run flushes)"},
+                          "in the pipelined run; the serial run flushes); a copy larger "
+                          "than L2 leaves its last part L2-resident for the kernel that "
+                          "follows, which is why the pipelined step can beat the "
+                          "flushed kernel-only step"},
             "gpu_launches": args.steps,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
