@@ -137,7 +137,8 @@ def test_fp8_forward_benchmark_workload(dev):
     _fp8_case(dev, qb, kb, vb, w.scale, w.causal, "fp8 " + w.name, config="fp8 " + w.name)
 
 
-@pytest.mark.parametrize("name", ["gate_B1_H32_L8192_d128", "B1_H32_L16384_d128_causal_qk3"])
+@pytest.mark.parametrize("name", ["gate_B1_H32_L8192_d128", "B1_H32_L16384_d128_causal_qk3",
+                                  "B1_H16_L32768_d64"])
 def test_fp8_forward_full_size_sampled(dev, name):
     import torch
     w = WORKLOADS[name]
