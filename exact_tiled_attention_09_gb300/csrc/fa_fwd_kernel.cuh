@@ -10,7 +10,7 @@
 // "FlashAttention 深度解析", third part, section 2.2 describes for Hopper,
 // re-targeted here to tcgen05 and tensor memory).
 //
-// Warp roles (320 threads; 352 at d = 64; 608 for FP8 at d = 64):
+// Warp roles (320 threads; 352 at d = 64):
 //   warp 0      MMA issuer and owner of the tensor memory: all 32 lanes run
 //               the loop and poll the barriers, one elected lane issues
 //               (d = 64: the products of Q tile 0 only)
@@ -22,9 +22,6 @@
 //               group cover quarters 2, 3, 0, 1)
 //   warps 6..9  softmax of Q tile 1
 //   warp 10     d = 64 only: MMA issuer of Q tile 1
-// FP8 at d = 64 splits every row's 128 key columns between two softmax warps
-// of one sub-partition: warps 2..17 are softmax (tile, column half, quarter)
-// and warp 18 is the MMA issuer of Q tile 1.
 //
 // d = 128, MMA order per K/V block j (each S_t buffer holds P_t after the
 // softmax, so S_t of block j+1 is issued only after O_t += P_t V_j):
@@ -89,7 +86,6 @@ enum : uint32_t {
   SITE_P = 5,
   SITE_O = 6,
   SITE_DRAIN = 7,
-  SITE_XCHG = 8,
 };
 
 template <int D, bool FP8 = false>
@@ -108,31 +104,17 @@ struct FwdCfg {
   // d = 64: P_t gets tensor-memory columns of its own, S_t is free as soon
   // as the softmax has read it, and each Q tile has its own MMA warp.
   static constexpr bool SPLIT_P = (D == 64);
-  // FP8 at d = 64: the 128 key columns of a row are split between two
-  // softmax warps of one sub-partition (four softmax warps per
-  // sub-partition, 92 registers a thread instead of a spilling 168), which
-  // combine their partial row maxima every block through shared memory.
-  // Measured on the L = 32768 workload: FP8 1162 -> 1210 TFLOP/s; the bf16
-  // d = 64 path measured 1254 without the split and 1240 with it, so it
-  // keeps whole rows per warp.
-  static constexpr int COL_SPLIT = (SPLIT_P && FP8) ? 2 : 1;
-  static constexpr int WARPS_PER_TILE = 4 * COL_SPLIT;
+  static constexpr int WARPS_PER_TILE = 4;  // softmax warps: one per TMEM lane quarter
   static constexpr int SOFTMAX_WARPS = TILES_PER_CTA * WARPS_PER_TILE;
-  static constexpr int KEYS_PER_WARP = BLOCK_N / COL_SPLIT;
   static constexpr int MMA_WARP_T1 = FIRST_SOFTMAX_WARP + SOFTMAX_WARPS;  // d = 64 only
   static constexpr int THREADS = 32 * (FIRST_SOFTMAX_WARP + SOFTMAX_WARPS + (SPLIT_P ? 1 : 0));
   static constexpr int Q_OFF = NSLOT * TILE_BYTES;
   static constexpr int BAR_OFF = Q_OFF + TILES_PER_CTA * QK_TILE_BYTES;
   // q_full, full[NSLOT], empty[NSLOT], s_full[2], p_full[2], o_done[2],
-  // drain[2] (one per MMA warp), s_free[2], xchg[2][4] (split rows: one
-  // per tile and quarter, the two column halves' warps arrive)
-  static constexpr int NBAR = 1 + 2 * NSLOT + 2 + 2 + 2 + 2 + 2 + (COL_SPLIT == 2 ? 8 : 0);
+  // drain[2] (one per MMA warp), s_free[2]
+  static constexpr int NBAR = 1 + 2 * NSLOT + 2 + 2 + 2 + 2 + 2;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-  // Split rows: partial row maxima (and at the end partial row sums), fp32
-  // [tile][block parity][column half][row]
-  static constexpr int XCH_OFF = MISC_OFF + 16;
-  static constexpr int XCH_BYTES = COL_SPLIT == 2 ? TILES_PER_CTA * 2 * 2 * BLOCK_M * 4 : 0;
-  static constexpr int SMEM_BYTES = XCH_OFF + XCH_BYTES + 1024;  // + alignment slack
+  static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + alignment slack
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   __host__ __device__ static constexpr uint32_t S_COL(int t) { return 128u * t; }
   __host__ __device__ static constexpr uint32_t O_COL(int t) {
@@ -165,6 +147,41 @@ struct FwdArgs {
   unsigned long long timeout_ns;
   int test_withhold_q;  // test hook: skip the Q copy so the first MMA wait runs out
 };
+
+// N chunks of 32 consecutive tensor-memory columns moved with one wide
+// instruction (measured: one x128 load of a score row instead of four x32
+// loads lifts the d = 64 forward by 4%).
+template <int N>
+__device__ __forceinline__ void tmem_ld_chunks(uint32_t taddr, uint32_t (&r)[N][32]) {
+  using W = uint32_t[N * 32];
+  if constexpr (N == 4)
+    tmem_ld128(taddr, reinterpret_cast<W&>(r));
+  else if constexpr (N == 2)
+    tmem_ld64(taddr, reinterpret_cast<W&>(r));
+  else
+    tmem_ld32(taddr, r[0]);
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_chunks(uint32_t taddr, uint32_t (&r)[N][32]) {
+  using W = uint32_t[N * 32];
+  if constexpr (N == 4)
+    tmem_st128(taddr, reinterpret_cast<W&>(r));
+  else if constexpr (N == 2)
+    tmem_st64(taddr, reinterpret_cast<W&>(r));
+  else
+    tmem_st32(taddr, r[0]);
+}
+// N chunks of 16 columns (packed bf16 P of 32 keys each).
+template <int N>
+__device__ __forceinline__ void tmem_st_pchunks(uint32_t taddr, uint32_t (&r)[N][16]) {
+  using W = uint32_t[N * 16];
+  if constexpr (N == 4)
+    tmem_st64(taddr, reinterpret_cast<W&>(r));
+  else if constexpr (N == 2)
+    tmem_st32(taddr, reinterpret_cast<W&>(r));
+  else
+    tmem_st16(taddr, r[0]);
+}
 
 // Number of K/V blocks Q tile t of this CTA needs (0 if the tile lies wholly
 // past the end of the sequence).  Causal: blocks whose first key exceeds the
@@ -206,10 +223,6 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
   auto bar_o = [&](int t) { return bars + 8u * (5 + 2 * C::NSLOT + t); };
   auto bar_drain = [&](int t) { return bars + 8u * (7 + 2 * C::NSLOT + t); };
   auto bar_sfree = [&](int t) { return bars + 8u * (9 + 2 * C::NSLOT + t); };
-  auto bar_xchg = [&](int t, int quarter) {
-    return bars + 8u * (11 + 2 * C::NSLOT + 4 * t + quarter);
-  };
-  float* const xch = reinterpret_cast<float*>(base_ptr + C::XCH_OFF);
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + C::MISC_OFF);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::MISC_OFF + 4);
 
@@ -272,8 +285,6 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
     for (int t = 0; t < TILES_PER_CTA; ++t) {
       mbar_init(bar_drain(t), 1);
       mbar_init(bar_sfree(t), C::WARPS_PER_TILE);  // one arrival per softmax warp
-      if constexpr (C::COL_SPLIT == 2)
-        for (int qr = 0; qr < 4; ++qr) mbar_init(bar_xchg(t, qr), 2);  // both column halves
     }
     *abort_flag = 0;
     fence_mbarrier_init();
@@ -529,28 +540,25 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
     }  // one MMA warp for both tiles (d = 128)
   } else {
     // ------------------------------------------------------------ softmax
-    // Warp (t, half, quarter): Q tile t, rows 32*quarter .. +31 (its TMEM
-    // lanes), key columns [half * KEYS_PER_WARP, (half + 1) * KEYS_PER_WARP)
-    // of every block (all 128, or one half each when rows are split, the two
-    // halves' warps sharing a sub-partition).
-    constexpr int NCH = C::KEYS_PER_WARP / 32;        // 32-column score chunks
-    constexpr int OCH = D / 32 / C::COL_SPLIT;        // 32-column O chunks
+    // Warp (t, quarter): Q tile t, rows 32*quarter .. +31 (its TMEM lanes),
+    // all 128 key columns of every block.
+    constexpr int NCH = BLOCK_N / 32;  // 32-column score chunks
+    constexpr int OCH = D / 32;        // 32-column O chunks
     const int sidx = warp - FIRST_SOFTMAX_WARP;
-    const int t = (sidx >> 2) >> (C::COL_SPLIT - 1);  // Q tile of this warp
-    const int half = (sidx >> 2) & (C::COL_SPLIT - 1);  // key-column half (split rows)
+    const int t = sidx >> 2;           // Q tile of this warp
     const int quarter = warp & 3;     // TMEM lanes this warp may access
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t s_col = C::S_COL(t) + static_cast<uint32_t>(half * C::KEYS_PER_WARP);
-    const uint32_t p_col = C::P_COL(t) + static_cast<uint32_t>(half * C::KEYS_PER_WARP / 2);
-    const uint32_t o_col = C::O_COL(t) + static_cast<uint32_t>(half * (D / C::COL_SPLIT));
+    const uint32_t s_col = C::S_COL(t);
+    const uint32_t p_col = C::P_COL(t);
+    const uint32_t o_col = C::O_COL(t);
     const int tile_row0 = row_base + t * BLOCK_M;
     const int q_row = tile_row0 + row;
     const int n_my = t == 0 ? n_blk0 : n_blk1;
     float sl2 = args.scale_log2;  // FP8: times s_q * s_k of the block, set per block
     const bool pos_scale = args.scale_log2 > 0.f;  // the block scales are positive
     float m = -INFINITY;  // running max of scale*log2e*s
-    float l = 0.f;        // running sum of P~ relative to m (split rows: this half's keys)
+    float l = 0.f;        // running sum of P~ relative to m
     bool ok = true;
     float sq = 1.f;
     float ks = 1.f;  // FP8: the scale of the next K block, loaded a block ahead
@@ -559,23 +567,6 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
         sq = args.q_scale[static_cast<size_t>(bh) * args.n_blocks + tile_row0 / BLOCK_M];
         ks = args.k_scale[static_cast<size_t>(bh) * args.n_blocks + jb];
       }
-    // Split rows: exchange a per-row value with the other column half's warp
-    // through shared memory, in slot [t][phase parity][half][row]; the
-    // barrier's phase `ph` completes when both warps have written.  Slots
-    // alternate by parity, so a warp cannot overwrite a value its partner
-    // has not read yet (it would first have to pass the next phase, which
-    // needs the partner's arrival).
-    auto exchange = [&](float mine, int ph, float& theirs) -> bool {
-      float* const slot = xch + (t * 2 + (ph & 1)) * 2 * BLOCK_M;
-      slot[half * BLOCK_M + row] = mine;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_xchg(t, quarter));
-      const bool wx = mbar_wait(bar_xchg(t, quarter), ph & 1, ctl, SITE_XCHG);
-      if (!__all_sync(0xffffffffu, wx)) return false;
-      theirs = slot[(half ^ 1) * BLOCK_M + row];
-      return true;
-    };
-
     for (int j = 0; j < n_my; ++j) {
       if constexpr (FP8) {
         sl2 = args.scale_log2 * sq * ks;
@@ -588,8 +579,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
       }
       tc_fence_after();
       uint32_t sr[NCH][32];
-#pragma unroll
-      for (int c = 0; c < NCH; ++c) tmem_ld32(lane_base + s_col + 32u * c, sr[c]);
+      tmem_ld_chunks<NCH>(lane_base + s_col, sr);
       tmem_wait_ld();
 #pragma unroll
       for (int c = 0; c < NCH; ++c) reg_fence32(sr[c]);
@@ -604,12 +594,11 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
       const int k0 = (jb + j) * BLOCK_N;
       const bool need_mask = (k0 + BLOCK_N > L) || (CAUSAL && k0 + BLOCK_N - 1 > tile_row0);
       if (need_mask) {
-        const int kw = k0 + half * C::KEYS_PER_WARP;
 #pragma unroll
         for (int c = 0; c < NCH; ++c)
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const int key = kw + c * 32 + e;
+            const int key = k0 + c * 32 + e;
             const bool masked = key >= L || (CAUSAL && key > q_row);
             if (masked) sr[c][e] = __float_as_uint(-INFINITY);
           }
@@ -646,16 +635,6 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
           }
         blk = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
       }
-      if constexpr (C::COL_SPLIT == 2) {
-        // The row max over the whole block: both halves end with the same
-        // value (max is exact and commutative).
-        float other;
-        if (!exchange(blk, j, other)) {
-          ok = false;
-          break;
-        }
-        blk = fmaxf(blk, other);
-      }
       const float m_new = fmaxf(m, blk);
       // Every row sees at least one unmasked key in every block it visits,
       // so m_new is finite here.
@@ -670,10 +649,11 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
       const uint64_t mul2 = f2_pack(mul, mul);
       const uint64_t negm2 = f2_pack(-m, -m);
       uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
-      // Keys 32c..32c+31 (of this warp's columns) pack into columns
-      // 16c..16c+15 of its P columns.  With separate P columns the stores
-      // wait until O_t += P_t V_{j-1} has completed (it reads the same
-      // columns); the exponentials run first, so that wait overlaps them.
+      // Keys 32c..32c+31 pack into columns 16c..16c+15 of the P columns.
+      // With separate P columns the stores (one wide store of all 64
+      // columns) wait until O_t += P_t V_{j-1} has completed (it reads the
+      // same columns); the exponentials run first, so that wait overlaps
+      // them.
       uint32_t pk[NCH][16];
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
@@ -700,8 +680,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
           }
           tc_fence_after();
         }
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) tmem_st16(lane_base + p_col + 16u * c, pk[c]);
+        tmem_st_pchunks<NCH>(lane_base + p_col, pk);
       }
       float s_lo, s_hi;
       f2_unpack(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), s_lo, s_hi);
@@ -711,13 +690,20 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
       // O_t is quiescent here: O_t += P_t V_{j-1} has completed (with separate
       // P columns the o_done wait above says so; otherwise the arrival on
       // s_full for this block came after it), and the next PV waits for p_full.
-      // Each column half's warp rescales its own share of O_t's columns.
       if (__any_sync(0xffffffffu, grew)) {
         // All of this warp's O_t columns in one round trip: issue every load,
         // wait once, scale in packed pairs, store back.
+        // (64 columns: one wide load and store; 128 columns: per-chunk
+        // stores after one round of loads, measured faster on the
+        // rescale-heavy d = 128 causal workload)
+        constexpr bool WIDE_O = OCH <= 2;
         uint32_t ov[OCH][32];
+        if constexpr (WIDE_O) {
+          tmem_ld_chunks<OCH>(lane_base + o_col, ov);
+        } else {
 #pragma unroll
-        for (int c = 0; c < OCH; ++c) tmem_ld32(lane_base + o_col + 32u * c, ov[c]);
+          for (int c = 0; c < OCH; ++c) tmem_ld32(lane_base + o_col + 32u * c, ov[c]);
+        }
         tmem_wait_ld();
         const uint64_t corr2 = f2_pack(corr, corr);
 #pragma unroll
@@ -732,8 +718,9 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
             ov[c][e] = __float_as_uint(a);
             ov[c][e + 1] = __float_as_uint(b);
           }
-          tmem_st32(lane_base + o_col + 32u * c, ov[c]);
+          if constexpr (!WIDE_O) tmem_st32(lane_base + o_col + 32u * c, ov[c]);
         }
+        if constexpr (WIDE_O) tmem_st_chunks<OCH>(lane_base + o_col, ov);
       }
       // One arrival per warp: every lane's tensor-memory stores are complete
       // (wait::st) and ordered (fence) before the warp syncs and lane 0
@@ -745,36 +732,33 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
     }
 
     const bool store = q_row < L;
-    if (ok && n_my > 0 && C::COL_SPLIT == 2) {
-      // Split rows: the row sum over both column halves (fp32 addition is
-      // commutative, so both warps hold the same l).
-      float other;
-      if (exchange(l, n_my, other))
-        l += other;
-      else
-        ok = false;
-    }
     if (ok && n_my > 0) {
-      // Epilogue: wait for the last O_t += P_t V, then O / l and LSE (each
-      // column half's warp writes its share of O's columns).
+      // Epilogue: wait for the last O_t += P_t V, then O / l and LSE.
       const bool w = mbar_wait(bar_o(t), C::SPLIT_P ? (n_my - 1) & 1 : 0, ctl, SITE_O);
       if (__all_sync(0xffffffffu, w)) {
         tc_fence_after();
         const float inv_l = 1.f / l;
         const float lse_row = (m + log2f(l)) * 0.69314718055994531f;
         const size_t row = static_cast<size_t>(bh) * L + q_row;
-        const int col0 = half * (D / C::COL_SPLIT);
+        constexpr bool WIDE_EPI = OCH <= 2;  // as for the rescale
+        uint32_t oall[WIDE_EPI ? OCH : 1][32];
+        if constexpr (WIDE_EPI) {
+          tmem_ld_chunks<OCH>(lane_base + o_col, oall);
+          tmem_wait_ld();
+        }
 #pragma unroll
         for (int c = 0; c < OCH; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(lane_base + o_col + 32u * c, ov);
-          tmem_wait_ld();
+          uint32_t (&ov)[32] = oall[WIDE_EPI ? c : 0];
+          if constexpr (!WIDE_EPI) {
+            tmem_ld32(lane_base + o_col + 32u * c, ov);
+            tmem_wait_ld();
+          }
           reg_fence32(ov);
           if constexpr (SPLIT) {
             // fp32 partial, normalised over this split's keys.
             if (store) {
               float4* dst = reinterpret_cast<float4*>(
-                  args.o_part + (static_cast<size_t>(split) * args.bh * L + row) * D + col0 + c * 32);
+                  args.o_part + (static_cast<size_t>(split) * args.bh * L + row) * D + c * 32);
 #pragma unroll
               for (int i = 0; i < 8; ++i)
                 dst[i] = make_float4(__uint_as_float(ov[4 * i]) * inv_l,
@@ -789,14 +773,14 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
               pk[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv_l,
                                   __uint_as_float(ov[2 * e + 1]) * inv_l);
             if (store) {
-              uint4* dst = reinterpret_cast<uint4*>(args.o + row * D + col0 + c * 32);
+              uint4* dst = reinterpret_cast<uint4*>(args.o + row * D + c * 32);
 #pragma unroll
               for (int i = 0; i < 4; ++i)
                 dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
             }
           }
         }
-        if (store && half == 0) {
+        if (store) {
           if constexpr (SPLIT)
             args.lse_part[static_cast<size_t>(split) * args.bh * L + row] = lse_row;
           else
@@ -808,11 +792,10 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
       // partial, weight exp(-inf) = 0 in the merge.
       const size_t row = static_cast<size_t>(bh) * L + q_row;
       float4* dst = reinterpret_cast<float4*>(
-          args.o_part + (static_cast<size_t>(split) * args.bh * L + row) * D +
-          half * (D / C::COL_SPLIT));
+          args.o_part + (static_cast<size_t>(split) * args.bh * L + row) * D);
 #pragma unroll
-      for (int i = 0; i < D / C::COL_SPLIT / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (half == 0) args.lse_part[static_cast<size_t>(split) * args.bh * L + row] = -INFINITY;
+      for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      args.lse_part[static_cast<size_t>(split) * args.bh * L + row] = -INFINITY;
     }
     tmem_wait_st();
   }
