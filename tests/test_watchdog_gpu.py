@@ -83,8 +83,8 @@ def test_wait_that_runs_out_is_reported_and_the_context_survives(dev, d, causal,
 
 @pytest.mark.parametrize("d,causal", [(64, False), (64, True), (128, False)])
 def test_fp8_wait_that_runs_out_is_reported(dev, d, causal):
-    # FP8 at d = 64 runs its own warp layout (two softmax warps per row, an
-    # MMA warp per tile): every role must still stop, drain and return
+    # FP8 at d = 64 runs two MMA warps (one per 128-query tile) and its own
+    # code path for the K scales: every role must still stop, drain and return
     import torch
     from tests.test_fp8_gpu import _fp8_case
     B, H, L = 2, 3, 600
