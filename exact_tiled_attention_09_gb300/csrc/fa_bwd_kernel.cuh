@@ -26,21 +26,21 @@
 //   dQ_i  = dS K_j                  (SS MMA, the same dS tile read MN-major,
 //                                    into the dP^T columns)
 //
-// and the gradient warps add dQ_i into an fp32 accumulator in global memory
-// (vector atomics; every key block of the head contributes to every dQ_i).
+// and dQ_i is added into an fp32 accumulator in global memory (tensor
+// reduce-adds; every key block of the head contributes to every dQ_i).
 // Post-pass: dQ = bf16(accumulator).
 //
-// Warp roles (320 threads):
+// Warp roles (576 threads):
 //   warp 0      MMA issuer, owner of the tensor memory (whole warp polls,
 //               one elected lane issues)
 //   warp 1      TMA producer: K_j, V_j once; Q_i and dO_i into a ring of
 //               stages (two at d = 128, three at d = 64); issues the dQ
 //               reduce-adds
-//   warps 2..9  gradient warps: warp w handles TMEM lanes 32*(w%4)..+31
-//               (its keys) and query columns 64*h..64*h+63, h = (w-2)/4
+//   warps 2..17 gradient warps: warp w handles TMEM lanes 32*(w%4)..+31
+//               (its keys) and query columns 32*h..32*h+31, h = (w-2)/4
 //
-// Tensor memory (512 columns): [0,128) S^T, then P^T as packed bf16 (half
-// h's 64 queries in columns 64h..64h+31); [128,256) dP^T, then dQ_i
+// Tensor memory (512 columns): [0,128) S^T, then P^T as packed bf16 (group
+// h's 32 queries in columns 32h..32h+15); [128,256) dP^T, then dQ_i
 // (d = 128; at d = 64 dQ_i has [384,448) of its own, so dP_{i+1} need not
 // wait for dQ_i to be copied out); [256,256+D) dV_j; [256+D,256+2D) dK_j.
 //
@@ -75,8 +75,16 @@
 
 namespace fa {
 
-constexpr int BWD_THREADS = 320;
+// Gradient warps: BWD_GRAD_GROUPS per TMEM lane quarter, each taking
+// 128 / BWD_GRAD_GROUPS query columns of S^T and dP^T and D / BWD_GRAD_GROUPS
+// columns of dQ, dK and dV.  Four groups (16 warps) keep four warps per
+// sub-partition on the element-wise phases, whose per-warp chains of
+// tensor-memory loads, exponentials and shared-memory stores are
+// latency-bound with two.
+constexpr int BWD_GRAD_GROUPS = 4;
+constexpr int BWD_GRAD_WARPS = 4 * BWD_GRAD_GROUPS;
 constexpr int BWD_FIRST_GRAD_WARP = 2;
+constexpr int BWD_THREADS = 32 * (BWD_FIRST_GRAD_WARP + BWD_GRAD_WARPS);
 constexpr int BWD_DS_BYTES = 128 * 128 * 2;  // dS^T tile, two 128 x 64 boxes
 
 // Wait sites of the backward kernel (bit index in the device status word).
@@ -129,6 +137,13 @@ struct BwdCfg {
   // dQ staging: 8 * D/64 boxes of 4 KB fill the Q and dO buffers exactly,
   // the first half in the Q buffer
   static constexpr int DQ_BOXES = 8 * BOXES;
+  // Packed bf16 P^T of gradient group h (queries CQ*h.., CQ = 128 / groups)
+  // lies in columns CQ*h..CQ*h + CQ/2 - 1 (over its own S^T columns): the
+  // 16 queries of MMA k-step kk start at this column.
+  __host__ __device__ static constexpr uint32_t p_col(int kk) {
+    return (128 / BWD_GRAD_GROUPS) * (16 * kk / (128 / BWD_GRAD_GROUPS)) +
+           (16 * kk % (128 / BWD_GRAD_GROUPS)) / 2;
+  }
   static_assert(DQ_BOXES * 4096 == 2 * TILE_BYTES, "dQ staging fills the Q/dO buffers");
   static constexpr uint32_t S_COL = 0;
   static constexpr uint32_t DP_COL = 128;
@@ -174,6 +189,42 @@ struct BwdPreArgs {
   long long rows;          // BH * Lp
   float scale;
 };
+
+// Tensor-memory moves of N consecutive 32-bit columns per lane in one
+// instruction (one wide access costs less than several narrow ones).
+__device__ __forceinline__ void bwd_tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+template <int N>
+__device__ __forceinline__ void bwd_tmem_ld(uint32_t taddr, uint32_t (&r)[N]) {
+  static_assert(N == 16 || N == 32 || N == 64, "16, 32 or 64 columns");
+  if constexpr (N == 64)
+    tmem_ld64(taddr, r);
+  else if constexpr (N == 32)
+    tmem_ld32(taddr, r);
+  else
+    bwd_tmem_ld16(taddr, r);
+}
+template <int N>
+__device__ __forceinline__ void bwd_tmem_st(uint32_t taddr, uint32_t (&r)[N]) {
+  static_assert(N == 16 || N == 32, "16 or 32 columns");
+  if constexpr (N == 32)
+    tmem_st32(taddr, r);
+  else
+    tmem_st16(taddr, r);
+}
+// Registers written by a tensor-memory load are not read before the wait.
+template <int N>
+__device__ __forceinline__ void reg_fence_n(uint32_t (&r)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
 
 constexpr int BWD_AUX_WARPS = 8;  // rows per block of the pre-pass
 
@@ -263,12 +314,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   };
   const uint32_t sDS = base + C::DS_OFF;
   uint8_t* const ds_ptr = base_ptr + C::DS_OFF;
-  // dQ staging box c of gradient warp (quarter, h), 32 rows x 32 floats:
-  // box b = (quarter*2 + h)*(D/64) + c at 4 KB steps from the Q buffer on.
-  auto dq_box_index = [](int quarter, int h, int c) { return (quarter * 2 + h) * (D / 64) + c; };
-  auto dq_box = [&](int st, int quarter, int h, int c) -> uint32_t {
-    return sQ(st) + dq_box_index(quarter, h, c) * 4096;
-  };
+  // dQ staging boxes of 32 rows x 32 floats at 4 KB steps from the Q
+  // buffer on: box b holds query rows 32*(b / (D/32)).. and dQ columns
+  // 32*(b % (D/32))..
+  auto dq_box = [&](int st, int b) -> uint32_t { return sQ(st) + b * 4096; };
   const uint32_t bars = base + C::BAR_OFF;
   const uint32_t bar_kv = bars;
   auto bar_fullq = [&](int s) { return bars + 8u * (1 + s); };
@@ -313,14 +362,14 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar_fullq(s), 1);
       mbar_init(bar_fulldo(s), 1);
-      mbar_init(bar_dqst(s), 8);  // one arrival per gradient warp: dQ staged
+      mbar_init(bar_dqst(s), BWD_GRAD_WARPS);  // one arrival per gradient warp: dQ staged
     }
     mbar_init(bar_s, 1);
     mbar_init(bar_dp, 1);
-    mbar_init(bar_p, 8);  // one arrival per gradient warp
-    mbar_init(bar_ds, 8);
+    mbar_init(bar_p, BWD_GRAD_WARPS);  // one arrival per gradient warp
+    mbar_init(bar_ds, BWD_GRAD_WARPS);
     mbar_init(bar_dq, 1);
-    mbar_init(bar_dqfree, 8);
+    mbar_init(bar_dqfree, BWD_GRAD_WARPS);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
@@ -392,12 +441,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       if (elect_one()) {
         const int qb = q_first + blk;
         for (int half = 0; half < 2; ++half) {
-          for (int quarter = 0; quarter < 4; ++quarter)
-            for (int hh = 0; hh < 2; ++hh)
-              for (int c = 0; c < D / 64; ++c)
-                if ((dq_box_index(quarter, hh, c) >= C::DQ_BOXES / 2) == (half == 1))
-                  tma_reduce_add_3d(&tmdQ, dq_box(st, quarter, hh, c), (D / 2) * hh + 32 * c,
-                                    qb * 128 + quarter * 32, bh);
+          for (int b = half * (C::DQ_BOXES / 2); b < (half + 1) * (C::DQ_BOXES / 2); ++b)
+            tma_reduce_add_3d(&tmdQ, dq_box(st, b), 32 * (b % (D / 32)),
+                              qb * 128 + 32 * (b / (D / 32)), bh);
           bulk_commit_group();
         }
         bulk_wait_group_read1();
@@ -494,8 +540,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         const uint64_t dod = sdesc_sw128(sdO(st), BOX, 1024);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + C::DV_COL, tmem + C::S_COL + 64 * (kk >> 2) + 8 * (kk & 3),
-                 dod + kk * (2048 >> 4), ID_DV, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::DV_COL, tmem + C::S_COL + C::p_col(kk), dod + kk * (2048 >> 4), ID_DV,
+                 (i > 0 || kk > 0) ? 1u : 0u);
       }
       __syncwarp();
       if (C::EARLY_S && i + 1 < n_i) {
@@ -542,10 +588,14 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ gradient warps
-    const int h = (warp - BWD_FIRST_GRAD_WARP) >> 2;  // query half: columns 64h..64h+63
-    const int quarter = warp & 3;                      // TMEM lanes this warp may access
-    const int r = quarter * 32 + lane;                 // TMEM lane: key row (S^T, dP^T,
-                                                       // dK, dV) or query row (dQ)
+    // Warp (quarter, h): TMEM lanes 32*quarter..+31 (its keys, or its queries
+    // for dQ), query columns CQ*h..CQ*h+CQ-1 of S^T and dP^T, and columns
+    // CW*h..CW*h+CW-1 of dQ_i, dK and dV.
+    constexpr int CQ = 128 / BWD_GRAD_GROUPS;
+    constexpr int CW = D / BWD_GRAD_GROUPS;
+    const int h = (warp - BWD_FIRST_GRAD_WARP) >> 2;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const int key = jblk * 128 + r;
     const bool key_ok = key < L;
@@ -553,57 +603,53 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const uint64_t sl2x2 = f2_pack(args.scale_log2, args.scale_log2);
     const uint64_t scale2 = f2_pack(args.scale, args.scale);
     auto terms_of = [&](int i) {
-      return reinterpret_cast<const float*>(rowterms(i % C::STAGES)) + 64 * h;
+      return reinterpret_cast<const float*>(rowterms(i % C::STAGES)) + CQ * h;
     };
-    float p[64];  // P^T of this warp's 64 queries, block of the last phase A
+    float p[CQ];  // P^T of this warp's queries, block of the last phase A
 
     // Phase A of block i: P^T = exp2(S^T * scale*log2e - lse*log2e), kept in
     // fp32 for dS and written to TMEM as bf16 (the A operand of
-    // dV += P^T dO).  The masks apply only on the causal diagonal block and
-    // in the last key block of a ragged L (both uniform across the CTA);
-    // elsewhere the per-element selects are compiled out.
+    // dV += P^T dO) over the first CQ/2 of the warp's own S^T columns.  The
+    // masks apply only on the causal diagonal block and in the last key
+    // block of a ragged L (both uniform across the CTA); elsewhere the
+    // per-element selects are compiled out.
     auto phase_a = [&](int i) -> bool {
       if (!__all_sync(0xffffffffu, mbar_wait(bar_s, i & 1, ctl, SITE_B_S))) return false;
       tc_fence_after();
       const int qb = q_first + i;
       const bool diag = CAUSAL && qb == jblk;
       const float* const terms = terms_of(i);
-      uint32_t sr[2][32];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) tmem_ld32(lane_base + C::S_COL + 64 * h + 32 * c, sr[c]);
+      uint32_t sr[CQ];
+      bwd_tmem_ld<CQ>(lane_base + C::S_COL + CQ * h, sr);
       tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < 2; ++c) reg_fence32(sr[c]);
+      reg_fence_n(sr);
       auto compute = [&](auto mask_tag) {
         constexpr bool MASK = decltype(mask_tag)::value;
+        uint32_t pk[CQ / 2];
+        const float4* nl = reinterpret_cast<const float4*>(terms);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const float4* nl = reinterpret_cast<const float4*>(terms + 32 * c);
-          uint32_t pk[16];
+        for (int e = 0; e < CQ; e += 4) {
+          const float4 a = nl[e >> 2];
+          float x0, x1, x2, x3;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl2x2,
+                           f2_pack(a.x, a.y)),
+                    x0, x1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), sl2x2,
+                           f2_pack(a.z, a.w)),
+                    x2, x3);
+          float pe[4] = {ex2_approx(x0), ex2_approx(x1), ex2_approx(x2), ex2_approx(x3)};
 #pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const float4 a = nl[e >> 2];
-            float x0, x1, x2, x3;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])),
-                             sl2x2, f2_pack(a.x, a.y)),
-                      x0, x1);
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][e + 2]), __uint_as_float(sr[c][e + 3])),
-                             sl2x2, f2_pack(a.z, a.w)),
-                      x2, x3);
-            float pe[4] = {ex2_approx(x0), ex2_approx(x1), ex2_approx(x2), ex2_approx(x3)};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              // causal: key r > query (64h + 32c + e + u) of the same block;
-              // keys past L (zero rows of K) never contribute.
-              if constexpr (MASK)
-                if ((diag && r > 64 * h + 32 * c + e + u) || !key_ok) pe[u] = 0.f;
-              p[32 * c + e + u] = pe[u];
-            }
-            pk[e >> 1] = pack_bf16x2(pe[0], pe[1]);
-            pk[(e >> 1) + 1] = pack_bf16x2(pe[2], pe[3]);
+          for (int u = 0; u < 4; ++u) {
+            // causal: key r > query (CQ*h + e + u) of the same block;
+            // keys past L (zero rows of K) never contribute.
+            if constexpr (MASK)
+              if ((diag && r > CQ * h + e + u) || !key_ok) pe[u] = 0.f;
+            p[e + u] = pe[u];
           }
-          tmem_st16(lane_base + C::S_COL + 64 * h + 16 * c, pk);
+          pk[e >> 1] = pack_bf16x2(pe[0], pe[1]);
+          pk[(e >> 1) + 1] = pack_bf16x2(pe[2], pe[3]);
         }
+        bwd_tmem_st<CQ / 2>(lane_base + C::S_COL + CQ * h, pk);
       };
       if (diag || tail_blk)
         compute(std::true_type{});
@@ -617,45 +663,40 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     };
 
     // Phase B of block i: dS^T = P^T (.) (scale * dP^T - scale * D), bf16
-    // into the 128B-swizzled dS tile: row = key, box h holds this half's 64
-    // queries.
+    // into the 128B-swizzled dS tile: row = key, box b holds queries
+    // 64b..64b+63, 16-byte unit u of row r at unit u ^ (r % 8).
     auto phase_b = [&](int i) -> bool {
       if (!__all_sync(0xffffffffu, mbar_wait(bar_dp, i & 1, ctl, SITE_B_DP))) return false;
       tc_fence_after();
       const float* const terms = terms_of(i);
-      uint32_t dr[2][32];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) tmem_ld32(lane_base + C::DP_COL + 64 * h + 32 * c, dr[c]);
+      uint32_t dr[CQ];
+      bwd_tmem_ld<CQ>(lane_base + C::DP_COL + CQ * h, dr);
       tmem_wait_ld();
+      reg_fence_n(dr);
+      const float4* nd = reinterpret_cast<const float4*>(terms + 128);
+      uint8_t* const row_ptr = ds_ptr + ((CQ * h) >> 6) * BOX + r * 128;
+      const int unit0 = ((CQ * h) & 63) >> 3;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) reg_fence32(dr[c]);
+      for (int e = 0; e < CQ; e += 8) {
+        uint32_t pk[4];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const float4* nd = reinterpret_cast<const float4*>(terms + 128 + 32 * c);
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 b = nd[e >> 2];
+        for (int g = 0; g < 8; g += 4) {
+          const float4 b = nd[(e + g) >> 2];
           float d0, d1, d2, d3;
-          f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(dr[c][e]), __uint_as_float(dr[c][e + 1])),
+          f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(dr[e + g]), __uint_as_float(dr[e + g + 1])),
                                   scale2, f2_pack(b.x, b.y)),
-                           f2_pack(p[32 * c + e], p[32 * c + e + 1])),
+                           f2_pack(p[e + g], p[e + g + 1])),
                     d0, d1);
-          f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(dr[c][e + 2]),
-                                          __uint_as_float(dr[c][e + 3])),
+          f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(dr[e + g + 2]),
+                                          __uint_as_float(dr[e + g + 3])),
                                   scale2, f2_pack(b.z, b.w)),
-                           f2_pack(p[32 * c + e + 2], p[32 * c + e + 3])),
+                           f2_pack(p[e + g + 2], p[e + g + 3])),
                     d2, d3);
-          pk[e >> 1] = pack_bf16x2(d0, d1);
-          pk[(e >> 1) + 1] = pack_bf16x2(d2, d3);
+          pk[g >> 1] = pack_bf16x2(d0, d1);
+          pk[(g >> 1) + 1] = pack_bf16x2(d2, d3);
         }
-        uint8_t* const row_ptr = ds_ptr + h * BOX + r * 128;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int unit = (4 * c + u) ^ (r & 7);
-          *reinterpret_cast<uint4*>(row_ptr + unit * 16) =
-              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-        }
+        const int unit = (unit0 + (e >> 3)) ^ (r & 7);
+        *reinterpret_cast<uint4*>(row_ptr + unit * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
       fence_proxy_async_smem();  // the MMA reads the tile through the async proxy
       tc_fence_before();
@@ -664,32 +705,30 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       return true;
     };
 
-    // Phase C of block i: copy this warp's D/2 columns of dQ_i out of TMEM
+    // Phase C of block i: copy this warp's CW columns of dQ_i out of TMEM
     // and release them, then stage them in block i's Q/dO buffers (every MMA
     // that read Q_i and dO_i is complete: the dq_full arrival follows them)
     // for the producer's reduce into the fp32 accumulator.  A box is 32 rows
-    // x 32 floats, 128-byte swizzled (16-byte chunk u of row r at chunk
+    // x 32 floats, 128-byte swizzled (16-byte unit u of row r at unit
     // u ^ (r % 8)); rows past L are skipped by the reduce.
     auto phase_c = [&](int i) -> bool {
       if (!__all_sync(0xffffffffu, mbar_wait(bar_dq, i & 1, ctl, SITE_B_DQ))) return false;
       tc_fence_after();
       const int st = i % C::STAGES;
-      uint32_t qv[D / 64][32];
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) tmem_ld32(lane_base + C::DQ_COL + (D / 2) * h + 32 * c, qv[c]);
+      uint32_t qv[CW];
+      bwd_tmem_ld<CW>(lane_base + C::DQ_COL + CW * h, qv);
       tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) reg_fence32(qv[c]);
+      reg_fence_n(qv);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dqfree);
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        uint8_t* const row_ptr = base_ptr + (dq_box(st, quarter, h, c) - base) + lane * 128;
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(row_ptr + ((u ^ (lane & 7)) * 16)) =
-              make_uint4(qv[c][4 * u], qv[c][4 * u + 1], qv[c][4 * u + 2], qv[c][4 * u + 3]);
+      for (int u = 0; u < CW / 4; ++u) {
+        const int col = CW * h + 4 * u;
+        uint8_t* const row_ptr =
+            base_ptr + (dq_box(st, quarter * (D / 32) + (col >> 5)) - base) + lane * 128;
+        *reinterpret_cast<uint4*>(row_ptr + ((((col & 31) >> 2) ^ (lane & 7)) * 16)) =
+            make_uint4(qv[4 * u], qv[4 * u + 1], qv[4 * u + 2], qv[4 * u + 3]);
       }
       fence_proxy_async_smem();  // the producer's reduce reads the stage via the async proxy
       __syncwarp();
@@ -721,23 +760,20 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const size_t row = static_cast<size_t>(bh) * L + key;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        const uint32_t col0 = (which == 0 ? C::DV_COL : C::DK_COL) + (D / 2) * h;
+        const uint32_t col0 = (which == 0 ? C::DV_COL : C::DK_COL) + CW * h;
         uint16_t* const out = which == 0 ? args.dv : args.dk;
+        uint32_t v[CW];
+        bwd_tmem_ld<CW>(lane_base + col0, v);
+        tmem_wait_ld();
+        reg_fence_n(v);
+        if (key_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(out + row * D + CW * h);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t v[32];
-          tmem_ld32(lane_base + col0 + 32 * c, v);
-          tmem_wait_ld();
-          reg_fence32(v);
-          if (key_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(out + row * D + (D / 2) * h + 32 * c);
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              dst[u] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * u]), __uint_as_float(v[8 * u + 1])),
-                                  pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3])),
-                                  pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5])),
-                                  pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7])));
-          }
+          for (int u = 0; u < CW / 8; ++u)
+            dst[u] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * u]), __uint_as_float(v[8 * u + 1])),
+                                pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3])),
+                                pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5])),
+                                pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7])));
         }
       }
     }
