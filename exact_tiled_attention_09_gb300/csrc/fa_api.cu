@@ -82,9 +82,10 @@ bool encode_map_u8(CUtensorMap* map, const void* ptr, int BH, int L, int D) {
 }
 
 // The fp32 dQ accumulator [BH, L, D] as a 3-D tensor (D, L, BH) with a
-// 32 x 32 x 1 box (128-byte rows) and the 128-byte swizzle: the target of
-// the backward kernel's reduce-adds.  Rows past L inside a head are out of
-// bounds, so a reduce of a ragged block never touches the next head.
+// 32 x 128 x 1 box (128-byte rows, one query block's rows of a 32-column
+// strip) and the 128-byte swizzle: the target of the backward kernel's
+// reduce-adds.  Rows past L inside a head are out of bounds, so a reduce of
+// a ragged block never touches the next head.
 bool encode_map_f32_acc(CUtensorMap* map, void* ptr, int BH, int L, int D) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
@@ -92,7 +93,7 @@ bool encode_map_f32_acc(CUtensorMap* map, void* ptr, int BH, int L, int D) {
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 4,
                                  static_cast<cuuint64_t>(L) * D * 4};
-  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t box[3] = {32, 128, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -46,7 +46,8 @@
 //
 // Order of the MMAs per query block (tcgen05 operations of one thread
 // complete in issue order, which the hand-offs rely on):
-//   d = 128: dP_i | wait P ready: dV_i | wait dS ready: dK_i, dQ_i | S_{i+1}
+//   d = 128: dP_i | wait P ready: dV_i | wait dS ready: dK_i, dQ_i (two
+//            column halves) | S_{i+1}
 //   d = 64:  dP_i | wait P ready: dV_i, S_{i+1} | wait dS ready: dK_i, dQ_i
 // and the gradient warps work on phases A (P), B (dS), C (dQ out) as
 // A(i) B(i) C(i) at d = 128 and A(0), then B(i) A(i+1) C(i) at d = 64, where
@@ -60,9 +61,13 @@
 // separate full barriers.  dQ_i leaves through the producer warp: the
 // gradient warps stage it in block i's Q and dO buffers (free once dQ_i is
 // final: every MMA that read them is complete) and arrive on dq_staged; the
-// producer issues the tensor reduce-adds as two groups, the boxes in the Q
-// buffer first, and refills the Q buffer (Q_{i+2}, needed first) as soon as
-// that group has been read, the dO buffer after the second.
+// producer issues the tensor reduce-adds as two groups, columns 0..d/2-1
+// (staged in the Q buffer) first, and refills the Q buffer (Q_{i+2}, needed
+// first) as soon as that group has been read, the dO buffer after the
+// second.  At d = 128 dQ_i is computed as two 64-column halves with a
+// commit each: the first half is staged, reduced and the Q buffer refilled
+// while the tensor core computes the second, and the Q copy enters the
+// copy engine before the second half's reduce.
 #pragma once
 
 #include <cuda.h>
@@ -124,8 +129,8 @@ struct BwdCfg {
   static constexpr int DS_OFF = STAGE_OFF + STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = DS_OFF + BWD_DS_BYTES;
   // kv_full, fullQ[S], fulldO[S], dq_staged[S], s_full, dp_full, p_ready,
-  // ds_ready, dq_full, dq_free, drain
-  static constexpr int NBAR = 1 + 3 * STAGES + 7;
+  // ds_ready, dq_full, dq_free, drain, dq_full2, dq_staged2[S]
+  static constexpr int NBAR = 1 + 3 * STAGES + 7 + 1 + STAGES;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   // The tiles need a 1024-byte aligned base; the launch adds as much slack
   // as the 227 KB budget leaves (up to 1024 bytes) and the kernel checks the
@@ -153,6 +158,11 @@ struct BwdCfg {
   // dP_{i+1} need not wait until dQ_i has been copied out (at d = 128 dQ_i
   // reuses dP_i's columns).
   static constexpr bool SPLIT_DQ = (D == 64);
+  // d = 128: dQ_i is computed as two 64-column halves with a commit each.
+  // The first half is staged (into the Q buffer) and its reduce started
+  // while the tensor core still computes the second, which brings the
+  // refill of the Q buffer for block i+2 forward.
+  static constexpr bool DQ_HALVES = (D == 128);
   static constexpr uint32_t DQ_COL = SPLIT_DQ ? 256 + 2 * D : DP_COL;
   static_assert(!SPLIT_DQ || DQ_COL + D <= 512, "tensor memory budget");
 };
@@ -314,9 +324,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   };
   const uint32_t sDS = base + C::DS_OFF;
   uint8_t* const ds_ptr = base_ptr + C::DS_OFF;
-  // dQ staging boxes of 32 rows x 32 floats at 4 KB steps from the Q
-  // buffer on: box b holds query rows 32*(b / (D/32)).. and dQ columns
-  // 32*(b % (D/32))..
+  // dQ staging: 32-row x 32-float pieces at 4 KB steps from the Q buffer
+  // on; piece 4*c + q holds dQ columns 32c..32c+31 of query rows 32q..32q+31,
+  // so the four pieces of a column strip c form one 128-row box of the
+  // reduce (16 KB), and columns 0..D/2-1 fill the Q buffer.
   auto dq_box = [&](int st, int b) -> uint32_t { return sQ(st) + b * 4096; };
   const uint32_t bars = base + C::BAR_OFF;
   const uint32_t bar_kv = bars;
@@ -333,6 +344,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   const uint32_t bar_dq = bar_s + 32;
   const uint32_t bar_dqfree = bar_s + 40;
   const uint32_t bar_drain = bar_s + 48;
+  const uint32_t bar_dq2 = bar_s + 56;  // second half of dQ_i (DQ_HALVES)
+  // dq_staged2 of stage s: the second half of the stage's dQ (DQ_HALVES)
+  auto bar_dqst2 = [&](int s) { return bar_s + 64 + 8u * s; };
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + C::MISC_OFF);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::MISC_OFF + 4);
 
@@ -371,6 +385,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     mbar_init(bar_dq, 1);
     mbar_init(bar_dqfree, BWD_GRAD_WARPS);
     mbar_init(bar_drain, 1);
+    mbar_init(bar_dq2, 1);
+    for (int s = 0; s < C::STAGES; ++s) mbar_init(bar_dqst2(s), BWD_GRAD_WARPS);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -435,35 +451,58 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     // buffer first.  Returns once the Q buffer has been read; the caller
     // waits for the rest (bulk_wait_group_read0) before reusing the dO
     // buffer.
+    auto reduce_half = [&](int blk, int half) {
+      const int st = blk % C::STAGES;
+      if (elect_one()) {
+        const int qb = q_first + blk;
+        for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c)
+          tma_reduce_add_3d(&tmdQ, dq_box(st, 4 * c), 32 * c, qb * 128, bh);
+        bulk_commit_group();
+      }
+      __syncwarp();
+    };
     auto reduce_block = [&](int blk) -> bool {
       const int st = blk % C::STAGES;
       if (!warp_wait(bar_dqst(st), use_parity(blk), SITE_B_DQST)) return false;
-      if (elect_one()) {
-        const int qb = q_first + blk;
-        for (int half = 0; half < 2; ++half) {
-          for (int b = half * (C::DQ_BOXES / 2); b < (half + 1) * (C::DQ_BOXES / 2); ++b)
-            tma_reduce_add_3d(&tmdQ, dq_box(st, b), 32 * (b % (D / 32)),
-                              qb * 128 + 32 * (b / (D / 32)), bh);
-          bulk_commit_group();
-        }
-        bulk_wait_group_read1();
-      }
+      reduce_half(blk, 0);
+      if (C::DQ_HALVES && !warp_wait(bar_dqst2(st), use_parity(blk), SITE_B_DQST)) return false;
+      reduce_half(blk, 1);
+      if (elect_one()) bulk_wait_group_read1();
       __syncwarp();
       return true;
     };
     // Block k reuses the stage of block k-2: Q_k once the first reduce group
-    // of block k-2 has been read, dO_k once the second has.
+    // of block k-2 has been read, dO_k once the second has.  At d = 128 the
+    // second group is issued only after the Q_k copy (measured: Q_k arrives
+    // sooner and the wait for S_k shrinks; at d = 64 the other order is
+    // faster).
     int q_loads = 0, do_loads = 0, reduced = 0;
     bool ok = true;
     for (int k = 0; k < n_i && ok; ++k) {
       if (k >= C::STAGES) {
-        ok = reduce_block(reduced);
-        if (!ok) break;
-        ++reduced;
+        if constexpr (C::DQ_HALVES) {
+          // the first half's reduce, then Q_k into the Q buffer it frees,
+          // ahead of the second half's reduce in the copy engine
+          ok = warp_wait(bar_dqst(reduced % C::STAGES), use_parity(reduced), SITE_B_DQST);
+          if (!ok) break;
+          reduce_half(reduced, 0);
+          if (elect_one()) bulk_wait_group_read0();
+          __syncwarp();
+        } else {
+          ok = reduce_block(reduced);
+          if (!ok) break;
+          ++reduced;
+        }
       }
       load_q(k);
       ++q_loads;
       if (k >= C::STAGES) {
+        if constexpr (C::DQ_HALVES) {
+          ok = warp_wait(bar_dqst2(reduced % C::STAGES), use_parity(reduced), SITE_B_DQST);
+          if (!ok) break;
+          reduce_half(reduced, 1);
+          ++reduced;
+        }
         if (elect_one()) bulk_wait_group_read0();
         __syncwarp();
       }
@@ -492,6 +531,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     constexpr uint32_t ID_DV = idesc_bf16_f32_ab(128, D, false, true);
     constexpr uint32_t ID_DK = idesc_bf16_f32_ab(128, D, false, true);
     constexpr uint32_t ID_DQ = idesc_bf16_f32_ab(128, D, true, true);
+    constexpr uint32_t ID_DQH = idesc_bf16_f32_ab(128, 64, true, true);
     // scores-like products: A and B K-major tiles of this CTA, K = d
     auto issue_kmajor = [&](uint32_t dcol, uint32_t a, uint32_t b, uint32_t bar) {
       if (elect_one()) {
@@ -566,11 +606,24 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         for (int kk = 0; kk < 8; ++kk)
           mma_ss(tmem + C::DK_COL, dsk + (((kk >> 2) * BOX + (kk & 3) * 32) >> 4),
                  qmn + kk * (2048 >> 4), ID_DK, (i > 0 || kk > 0) ? 1u : 0u);
+        if constexpr (C::DQ_HALVES) {
+          // columns 64h..64h+63 of dQ_i from box h of K (MN-major, N = 64)
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + C::DQ_COL, dsm + kk * (2048 >> 4), kmn + kk * (2048 >> 4), ID_DQ,
-                 kk > 0 ? 1u : 0u);
-        mma_commit(bar_dq);
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint64_t kh = sdesc_sw128(sK + hh * BOX, BOX, 1024);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss(tmem + C::DQ_COL + 64 * hh, dsm + kk * (2048 >> 4), kh + kk * (2048 >> 4),
+                     ID_DQH, kk > 0 ? 1u : 0u);
+            mma_commit(hh == 0 ? bar_dq : bar_dq2);
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + C::DQ_COL, dsm + kk * (2048 >> 4), kmn + kk * (2048 >> 4), ID_DQ,
+                   kk > 0 ? 1u : 0u);
+          mma_commit(bar_dq);
+        }
       }
       __syncwarp();
       if (!C::EARLY_S && i + 1 < n_i) {
@@ -705,34 +758,60 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       return true;
     };
 
-    // Phase C of block i: copy this warp's CW columns of dQ_i out of TMEM
-    // and release them, then stage them in block i's Q/dO buffers (every MMA
+    // Phase C of block i: copy this warp's columns of dQ_i out of TMEM and
+    // release them, then stage them in block i's Q/dO buffers (every MMA
     // that read Q_i and dO_i is complete: the dq_full arrival follows them)
-    // for the producer's reduce into the fp32 accumulator.  A box is 32 rows
-    // x 32 floats, 128-byte swizzled (16-byte unit u of row r at unit
-    // u ^ (r % 8)); rows past L are skipped by the reduce.
-    auto phase_c = [&](int i) -> bool {
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_dq, i & 1, ctl, SITE_B_DQ))) return false;
-      tc_fence_after();
-      const int st = i % C::STAGES;
-      uint32_t qv[CW];
-      bwd_tmem_ld<CW>(lane_base + C::DQ_COL + CW * h, qv);
-      tmem_wait_ld();
-      reg_fence_n(qv);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_dqfree);
-#pragma unroll
-      for (int u = 0; u < CW / 4; ++u) {
-        const int col = CW * h + 4 * u;
+    // for the producer's reduce into the fp32 accumulator.  Pieces are 32
+    // rows x 32 floats, 128-byte swizzled (16-byte unit u of row r at unit
+    // u ^ (r % 8)); rows past L are skipped by the reduce.  With DQ_HALVES
+    // the two column halves are copied and staged one after the other, each
+    // as soon as its product has completed (half 0 lands in the Q buffer).
+    auto stage_dq = [&](int st, const uint32_t* qv, int col0, int ncols) {
+#pragma unroll 4
+      for (int u = 0; u < ncols / 4; ++u) {
+        const int col = col0 + 4 * u;
         uint8_t* const row_ptr =
-            base_ptr + (dq_box(st, quarter * (D / 32) + (col >> 5)) - base) + lane * 128;
+            base_ptr + (dq_box(st, (col >> 5) * 4 + quarter) - base) + lane * 128;
         *reinterpret_cast<uint4*>(row_ptr + ((((col & 31) >> 2) ^ (lane & 7)) * 16)) =
             make_uint4(qv[4 * u], qv[4 * u + 1], qv[4 * u + 2], qv[4 * u + 3]);
       }
       fence_proxy_async_smem();  // the producer's reduce reads the stage via the async proxy
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_dqst(st));
+    };
+    auto phase_c = [&](int i) -> bool {
+      const int st = i % C::STAGES;
+      if constexpr (C::DQ_HALVES) {
+        constexpr int HW = 64 / BWD_GRAD_GROUPS;  // columns per warp and half
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          if (!__all_sync(0xffffffffu, mbar_wait(hh == 0 ? bar_dq : bar_dq2, i & 1, ctl, SITE_B_DQ)))
+            return false;
+          tc_fence_after();
+          uint32_t qv[HW];
+          bwd_tmem_ld<HW>(lane_base + C::DQ_COL + 64 * hh + HW * h, qv);
+          tmem_wait_ld();
+          reg_fence_n(qv);
+          if (hh == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_dqfree);
+          }
+          stage_dq(st, qv, 64 * hh + HW * h, HW);
+          if (lane == 0) mbar_arrive(hh == 0 ? bar_dqst(st) : bar_dqst2(st));
+        }
+      } else {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_dq, i & 1, ctl, SITE_B_DQ))) return false;
+        tc_fence_after();
+        uint32_t qv[CW];
+        bwd_tmem_ld<CW>(lane_base + C::DQ_COL + CW * h, qv);
+        tmem_wait_ld();
+        reg_fence_n(qv);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_dqfree);
+        stage_dq(st, qv, CW * h, CW);
+        if (lane == 0) mbar_arrive(bar_dqst(st));
+      }
       return true;
     };
 
