@@ -127,13 +127,37 @@ int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
+// Launch `kernel` as a programmatic dependant of the previous work on
+// `stream` (it may start while that work drains and must wait for it with
+// griddepcontrol.wait before reading its results).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 template <int D>
 int launch_merge(const FwdArgs& args, int n_splits, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(args.bh) * args.L;
   const dim3 grid(static_cast<unsigned>((rows + MERGE_WARPS - 1) / MERGE_WARPS));
-  fa_merge_kernel<D><<<grid, MERGE_WARPS * 32, 0, stream>>>(args.o_part, args.lse_part, args.o,
-                                                            args.lse, rows, n_splits);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+  // a programmatic dependant of the split pass: launched while it drains,
+  // it waits for that grid before reading the partials
+  const float* o_part = args.o_part;
+  const float* lse_part = args.lse_part;
+  return launch_dependent(fa_merge_kernel<D>, grid, dim3(MERGE_WARPS * 32), 0, stream, o_part,
+                          lse_part, args.o, args.lse, rows, n_splits) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_LAUNCH;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -253,17 +277,26 @@ int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
   static bool configured[kMaxDevices] = {};
   static std::mutex mu;
   if (!configure_once(kernel, smem, dev, configured, mu)) return FA_ERR_LAUNCH;
-  const dim3 pre_grid(static_cast<unsigned>((pre.rows + BWD_AUX_WARPS - 1) / BWD_AUX_WARPS));
+  constexpr long long pre_rows_per_block = BWD_AUX_WARPS * BWD_PRE_ROWS;
+  const dim3 pre_grid(
+      static_cast<unsigned>((pre.rows + pre_rows_per_block - 1) / pre_rows_per_block));
   fa_bwd_pre_kernel<D><<<pre_grid, BWD_AUX_WARPS * 32, 0, stream>>>(pre);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  // The gradient kernel and the post-pass are programmatic dependants of the
+  // kernel before them: each starts while that one drains and waits for it
+  // before reading its results.
   const dim3 grid(static_cast<unsigned>(args.bh) * static_cast<unsigned>(args.n_kv));
-  kernel<<<grid, BWD_THREADS, smem, stream>>>(mq, mk, mv, mdo, mdq, args);
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  if (launch_dependent(kernel, grid, dim3(BWD_THREADS), smem, stream, mq, mk, mv, mdo, mdq,
+                       args) != cudaSuccess)
+    return FA_ERR_LAUNCH;
   const long long n4 = static_cast<long long>(args.bh) * args.L * D / 4;
   const long long blocks = (n4 + 255) / 256;
-  const dim3 post_grid(static_cast<unsigned>(blocks < 152 * 16 ? blocks : 152 * 16));
-  fa_bwd_post_kernel<<<post_grid, 256, 0, stream>>>(args.dq_acc, dq, n4);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+  const dim3 post_grid(static_cast<unsigned>(blocks < 152 * 4 ? blocks : 152 * 4));
+  const float* acc = args.dq_acc;
+  return launch_dependent(fa_bwd_post_kernel, post_grid, dim3(256), 0, stream, acc, dq, n4) ==
+                 cudaSuccess
+             ? FA_OK
+             : FA_ERR_LAUNCH;
 }
 
 }  // namespace

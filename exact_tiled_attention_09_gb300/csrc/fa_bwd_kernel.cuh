@@ -76,6 +76,7 @@
 #include <cstdint>
 #include <type_traits>
 
+#include "pdl.cuh"
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -236,62 +237,102 @@ __device__ __forceinline__ void reg_fence_n(uint32_t (&r)[N]) {
   for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
 }
 
-constexpr int BWD_AUX_WARPS = 8;  // rows per block of the pre-pass
+constexpr int BWD_AUX_WARPS = 8;  // warps per block of the pre-pass
+constexpr int BWD_PRE_ROWS = 4;   // rows per warp of the pre-pass
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// Pre-pass, one warp per row of [BH, Lp]: D_i = <dO_i, O_i> (fp32, bf16
-// inputs), stored as -scale * D_i, and -lse_i * log2(e); rows past L get
-// the values that make them vanish in the main kernel (P = 0, dS = 0).  It
-// also zeroes the dQ accumulator row.
+// Pre-pass, one warp per BWD_PRE_ROWS consecutive rows of [BH, Lp]:
+// D_i = <dO_i, O_i> (fp32, bf16 inputs), stored as -scale * D_i, and
+// -lse_i * log2(e); rows past L get the values that make them vanish in the
+// main kernel (P = 0, dS = 0).  It also zeroes the dQ accumulator rows.  The
+// loads of all the warp's rows are issued before any is used (more bytes in
+// flight per warp: the kernel is bound by HBM).  The main kernel is its
+// programmatic dependant: it is launched as the last blocks of this grid
+// exit (no early trigger: a gradient CTA resident early would take the
+// registers that blocks of this pass need on its SM).
 template <int D>
 __global__ void __launch_bounds__(BWD_AUX_WARPS * 32) fa_bwd_pre_kernel(const BwdPreArgs a) {
-  const long long row = static_cast<long long>(blockIdx.x) * BWD_AUX_WARPS + (threadIdx.x >> 5);
+  using Vec = typename std::conditional<D == 64, uint32_t, uint2>::type;
+  const long long row0 =
+      (static_cast<long long>(blockIdx.x) * BWD_AUX_WARPS + (threadIdx.x >> 5)) * BWD_PRE_ROWS;
   const int lane = threadIdx.x & 31;
-  if (row >= a.rows) return;
-  const long long bh = row / a.Lp;
-  const int q = static_cast<int>(row - bh * a.Lp);
-  if (q >= a.L) {
-    if (lane == 0) {
-      a.nlse2[row] = -INFINITY;
-      a.nds[row] = 0.f;
+  Vec ow[BWD_PRE_ROWS], dw[BWD_PRE_ROWS];
+  bool live[BWD_PRE_ROWS];
+#pragma unroll
+  for (int k = 0; k < BWD_PRE_ROWS; ++k) {
+    const long long row = row0 + k;
+    const long long bh = row / a.Lp;
+    const int q = static_cast<int>(row - bh * a.Lp);
+    live[k] = row < a.rows && q < a.L;
+    if (live[k]) {
+      const size_t src = (static_cast<size_t>(bh) * a.L + q) * D;
+      ow[k] = reinterpret_cast<const Vec*>(a.o + src)[lane];
+      dw[k] = reinterpret_cast<const Vec*>(a.dout + src)[lane];
+      if constexpr (D == 64)
+        reinterpret_cast<float2*>(a.dq_acc + src)[lane] = make_float2(0.f, 0.f);
+      else
+        reinterpret_cast<float4*>(a.dq_acc + src)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    return;
-  }
-  const size_t src = (static_cast<size_t>(bh) * a.L + q) * D;
-  float acc;
-  if constexpr (D == 64) {
-    const uint32_t ow = reinterpret_cast<const uint32_t*>(a.o + src)[lane];
-    const uint32_t dw = reinterpret_cast<const uint32_t*>(a.dout + src)[lane];
-    acc = fmaf(bf16_hi(ow), bf16_hi(dw), bf16_lo(ow) * bf16_lo(dw));
-    reinterpret_cast<float2*>(a.dq_acc + src)[lane] = make_float2(0.f, 0.f);
-  } else {
-    const uint2 ow = reinterpret_cast<const uint2*>(a.o + src)[lane];
-    const uint2 dw = reinterpret_cast<const uint2*>(a.dout + src)[lane];
-    acc = bf16_lo(ow.x) * bf16_lo(dw.x);
-    acc = fmaf(bf16_hi(ow.x), bf16_hi(dw.x), acc);
-    acc = fmaf(bf16_lo(ow.y), bf16_lo(dw.y), acc);
-    acc = fmaf(bf16_hi(ow.y), bf16_hi(dw.y), acc);
-    reinterpret_cast<float4*>(a.dq_acc + src)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) {
-    a.nlse2[row] = -a.lse[static_cast<size_t>(bh) * a.L + q] * 1.4426950408889634f;
-    a.nds[row] = -a.scale * acc;
+  for (int k = 0; k < BWD_PRE_ROWS; ++k) {
+    const long long row = row0 + k;
+    if (row >= a.rows) break;
+    float acc = 0.f;
+    if (live[k]) {
+      if constexpr (D == 64) {
+        const uint32_t o1 = ow[k], d1 = dw[k];
+        acc = fmaf(bf16_hi(o1), bf16_hi(d1), bf16_lo(o1) * bf16_lo(d1));
+      } else {
+        const uint2 o2 = ow[k], d2 = dw[k];
+        acc = bf16_lo(o2.x) * bf16_lo(d2.x);
+        acc = fmaf(bf16_hi(o2.x), bf16_hi(d2.x), acc);
+        acc = fmaf(bf16_lo(o2.y), bf16_lo(d2.y), acc);
+        acc = fmaf(bf16_hi(o2.y), bf16_hi(d2.y), acc);
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) {
+      const long long bh = row / a.Lp;
+      const int q = static_cast<int>(row - bh * a.Lp);
+      if (live[k]) {
+        a.nlse2[row] = -a.lse[static_cast<size_t>(bh) * a.L + q] * 1.4426950408889634f;
+        a.nds[row] = -a.scale * acc;
+      } else {
+        a.nlse2[row] = -INFINITY;
+        a.nds[row] = 0.f;
+      }
+    }
   }
 }
 
-// Post-pass: dQ = bf16(accumulator), four elements per thread and step.
+// Post-pass: dQ = bf16(accumulator), four elements per thread and step,
+// BWD_POST_UNROLL steps' loads issued together.  Launched as a dependant of
+// the main kernel: it waits for that grid before reading the accumulator.
+constexpr int BWD_POST_UNROLL = 4;
 __global__ void __launch_bounds__(256) fa_bwd_post_kernel(const float* __restrict__ acc,
                                                           uint16_t* __restrict__ dq,
                                                           long long n4) {
+  pdl_wait();
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
-       i += stride) {
-    const float4 v = reinterpret_cast<const float4*>(acc)[i];
-    reinterpret_cast<uint2*>(dq)[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+  for (long long i0 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < n4;
+       i0 += stride * BWD_POST_UNROLL) {
+    float4 v[BWD_POST_UNROLL];
+#pragma unroll
+    for (int u = 0; u < BWD_POST_UNROLL; ++u) {
+      const long long i = i0 + u * stride;
+      if (i < n4) v[u] = reinterpret_cast<const float4*>(acc)[i];
+    }
+#pragma unroll
+    for (int u = 0; u < BWD_POST_UNROLL; ++u) {
+      const long long i = i0 + u * stride;
+      if (i < n4)
+        reinterpret_cast<uint2*>(dq)[i] =
+            make_uint2(pack_bf16x2(v[u].x, v[u].y), pack_bf16x2(v[u].z, v[u].w));
+    }
   }
 }
 
@@ -422,6 +463,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
     }
     __syncwarp();
+    // The per-query terms and the zeroed dQ accumulator come from the
+    // pre-pass, which may still be running (programmatic launch).
+    pdl_wait();
     auto load_q = [&](int blk) {
       const int st = blk % C::STAGES;
       if (elect_one()) {

@@ -20,6 +20,7 @@
 
 #include <cstdint>
 
+#include "pdl.cuh"
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -32,6 +33,7 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32)
                     uint16_t* __restrict__ o, float* __restrict__ lse, int64_t rows,
                     int n_splits) {
   constexpr int PER_LANE = D / 32;
+  pdl_wait();  // the partials come from the split pass (programmatic launch)
   const int64_t row = static_cast<int64_t>(blockIdx.x) * MERGE_WARPS + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
