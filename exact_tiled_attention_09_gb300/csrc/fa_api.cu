@@ -286,7 +286,7 @@ int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
   // kernel before them: each starts while that one drains and waits for it
   // before reading its results.
   const dim3 grid(static_cast<unsigned>(args.bh) * static_cast<unsigned>(args.n_kv));
-  if (launch_dependent(kernel, grid, dim3(BWD_THREADS), smem, stream, mq, mk, mv, mdo, mdq,
+  if (launch_dependent(kernel, grid, dim3(BwdCfg<D>::THREADS), smem, stream, mq, mk, mv, mdo, mdq,
                        args) != cudaSuccess)
     return FA_ERR_LAUNCH;
   const long long n4 = static_cast<long long>(args.bh) * args.L * D / 4;

@@ -90,7 +90,6 @@ namespace fa {
 constexpr int BWD_GRAD_GROUPS = 4;
 constexpr int BWD_GRAD_WARPS = 4 * BWD_GRAD_GROUPS;
 constexpr int BWD_FIRST_GRAD_WARP = 2;
-constexpr int BWD_THREADS = 32 * (BWD_FIRST_GRAD_WARP + BWD_GRAD_WARPS);
 constexpr int BWD_DS_BYTES = 128 * 128 * 2;  // dS^T tile, two 128 x 64 boxes
 
 // Wait sites of the backward kernel (bit index in the device status word).
@@ -164,6 +163,14 @@ struct BwdCfg {
   // while the tensor core still computes the second, which brings the
   // refill of the Q buffer for block i+2 forward.
   static constexpr bool DQ_HALVES = (D == 128);
+  // d = 64: four more warps (one per TMEM lane quarter, after the gradient
+  // warps) copy dQ_i out of tensor memory and stage it, so that the
+  // gradient warps go from dS_i straight to P of the next block.
+  static constexpr int DQ_WARPS = (D == 64) ? 4 : 0;
+  static constexpr int FIRST_DQ_WARP = BWD_FIRST_GRAD_WARP + BWD_GRAD_WARPS;
+  static constexpr int THREADS = 32 * (FIRST_DQ_WARP + DQ_WARPS);
+  // arrivals on dq_free and dq_staged: the warps that copy dQ out
+  static constexpr int DQ_COPIERS = DQ_WARPS ? DQ_WARPS : BWD_GRAD_WARPS;
   static constexpr uint32_t DQ_COL = SPLIT_DQ ? 256 + 2 * D : DP_COL;
   static_assert(!SPLIT_DQ || DQ_COL + D <= 512, "tensor memory budget");
 };
@@ -338,7 +345,7 @@ __global__ void __launch_bounds__(256) fa_bwd_post_kernel(const float* __restric
 
 // Main backward kernel: one CTA per (head, key block); see the file comment.
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(BWD_THREADS, 1)
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                   const __grid_constant__ CUtensorMap tmdQ, const BwdArgs args) {
@@ -417,17 +424,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar_fullq(s), 1);
       mbar_init(bar_fulldo(s), 1);
-      mbar_init(bar_dqst(s), BWD_GRAD_WARPS);  // one arrival per gradient warp: dQ staged
+      mbar_init(bar_dqst(s), C::DQ_COPIERS);  // one arrival per copying warp: dQ staged
     }
     mbar_init(bar_s, 1);
     mbar_init(bar_dp, 1);
     mbar_init(bar_p, BWD_GRAD_WARPS);  // one arrival per gradient warp
     mbar_init(bar_ds, BWD_GRAD_WARPS);
     mbar_init(bar_dq, 1);
-    mbar_init(bar_dqfree, BWD_GRAD_WARPS);
+    mbar_init(bar_dqfree, C::DQ_COPIERS);
     mbar_init(bar_drain, 1);
     mbar_init(bar_dq2, 1);
-    for (int s = 0; s < C::STAGES; ++s) mbar_init(bar_dqst2(s), BWD_GRAD_WARPS);
+    for (int s = 0; s < C::STAGES; ++s) mbar_init(bar_dqst2(s), C::DQ_COPIERS);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -515,8 +522,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       __syncwarp();
       return true;
     };
-    // Block k reuses the stage of block k-2: Q_k once the first reduce group
-    // of block k-2 has been read, dO_k once the second has.  At d = 128 the
+    // Block k reuses the stage of block k - STAGES: Q_k once the first reduce
+    // group of that block has been read, dO_k once the second has.  At d = 128 the
     // second group is issued only after the Q_k copy (measured: Q_k arrives
     // sooner and the wait for S_k shrinks; at d = 64 the other order is
     // faster).
@@ -682,6 +689,41 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         mbar_wait_drain(bar_drain, 0, args.timeout_ns);
       }
       __syncwarp();
+    }
+  } else if (C::DQ_WARPS > 0 && warp >= C::FIRST_DQ_WARP) {
+    // ------------------------------------------------------------ dQ warps
+    // Warp q (TMEM lanes 32q..32q+31 = query rows of dQ_i): per block, dQ_i
+    // out of tensor memory, 32 columns at a time, then into the staging
+    // pieces of the block's Q/dO buffers (every MMA that read Q_i and dO_i is
+    // complete: the dq_full arrival follows them).
+    const int quarter = warp & 3;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    bool ok = true;
+    for (int i = 0; i < n_i && ok; ++i) {
+      const int st = i % C::STAGES;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_dq, i & 1, ctl, SITE_B_DQ));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t qv[D / 32][32];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_base + C::DQ_COL + 32 * c, qv[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) reg_fence32(qv[c]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_dqfree);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint8_t* const row_ptr = base_ptr + (dq_box(st, c * 4 + quarter) - base) + lane * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(row_ptr + ((u ^ (lane & 7)) * 16)) =
+              make_uint4(qv[c][4 * u], qv[c][4 * u + 1], qv[c][4 * u + 2], qv[c][4 * u + 3]);
+      }
+      fence_proxy_async_smem();  // the producer's reduce reads the stage via the async proxy
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_dqst(st));
     }
   } else {
     // ------------------------------------------------------------ gradient warps
@@ -867,7 +909,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       for (int i = 0; i < n_i && ok; ++i) {
         ok = phase_b(i);
         if (ok && i + 1 < n_i) ok = phase_a(i + 1);
-        if (ok) ok = phase_c(i);
+        if (C::DQ_WARPS == 0 && ok) ok = phase_c(i);
       }
     } else {
       for (int i = 0; i < n_i && ok; ++i) {
@@ -878,7 +920,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     }
 
     // Epilogue: the last dq_full arrival came after every MMA of the CTA, so
-    // dV_j and dK_j are final.  bf16 (round to nearest even), rows < L.
+    // dV_j and dK_j are final (the gradient warps wait for it here when the
+    // dQ warps copy dQ out).  bf16 (round to nearest even), rows < L.
+    if (C::DQ_WARPS > 0 && ok) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_dq, (n_i - 1) & 1, ctl, SITE_B_DQ));
+      if (ok) tc_fence_after();
+    }
     if (ok) {
       const size_t row = static_cast<size_t>(bh) * L + key;
 #pragma unroll
