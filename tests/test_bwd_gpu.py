@@ -242,3 +242,31 @@ def test_bwd_outputs_fully_overwritten_and_bounded(dev):
 
 def test_bwd_status_after_runs_is_ok(dev):
     assert fa.fa_device_status(None, clear=False) == fa.FA_OK
+
+
+def test_bwd_back_to_back_calls_share_one_workspace(dev):
+    # Two backward calls on one (non-default) stream with no host sync
+    # between them and one shared workspace: the gradient kernel and the
+    # dQ conversion are programmatic dependants of the kernel before them,
+    # so the second call's pre-pass (which zeroes the shared dQ accumulator)
+    # must still wait for the first call's conversion to finish reading it.
+    import torch
+    L, d = 640, 128
+    cases = []
+    for seed in (3700, 3701):
+        qb, kb, vb = make_custom(1, 3, L, d, seed)
+        dob = make_custom_grad_out(1, 3, L, d, seed)
+        cases.append((qb, kb, vb, dob))
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(1, 3, L, d), dtype=torch.uint8, device=dev)
+    side = torch.cuda.Stream(device=dev)
+    outs = []
+    with torch.cuda.stream(side):
+        for qb, kb, vb, dob in cases:
+            q, k, v, do = (to_device(x, dev) for x in (qb, kb, vb, dob))
+            o, lse = fa.forward(q, k, v, scale=0.1, causal=True, stream=side)
+            outs.append(fa.backward(q, k, v, o, lse, do, scale=0.1, causal=True, workspace=ws,
+                                    stream=side))
+    side.synchronize()
+    for (qb, kb, vb, dob), got in zip(cases, outs):
+        ref = oracle.attention_bwd(_f64(qb), _f64(kb), _f64(vb), _f64(dob), 0.1, True)
+        check_grads_per_head([from_device(t) for t in got], ref, "back to back")

@@ -102,3 +102,24 @@ def test_splitkv_workspace_reuse(dev):
         o_ref, lse_ref, a_ref = oracle_forward(_f64(qb), _f64(kb), _f64(vb), 0.1, bool(seed % 2))
         check_parity(from_device(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
                      f"reuse seed {seed}", absv_ref=a_ref)
+
+
+def test_splitkv_back_to_back_calls_share_one_workspace(dev):
+    # Two split-KV calls on one stream without a host sync, one workspace:
+    # the merge is a programmatic dependant of its split pass; the second
+    # call's split pass must not overwrite partials the first merge still
+    # reads.
+    import torch
+    L, d, S = 900, 64, 5
+    ws = torch.empty(fa.fa_splitkv_workspace_bytes(2, 2, L, d, S), dtype=torch.uint8,
+                     device=dev)
+    cases = [make_custom(2, 2, L, d, seed=seed) for seed in (31, 32)]
+    outs = []
+    for qb, kb, vb in cases:
+        q, k, v = (to_device(x, dev) for x in (qb, kb, vb))
+        outs.append(fa.forward_splitkv(q, k, v, S, scale=0.125, causal=False, workspace=ws))
+    torch.cuda.synchronize()
+    for (qb, kb, vb), (o, lse) in zip(cases, outs):
+        o_ref, lse_ref, a_ref = oracle_forward(_f64(qb), _f64(kb), _f64(vb), 0.125, False)
+        check_parity(from_device(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
+                     "back to back", absv_ref=a_ref)
