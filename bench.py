@@ -393,16 +393,10 @@ def backward_line(fa, w, t, peaks):
             "gradient_kernel_dram_bytes": traffic, "traffic_source": src}
 
 
-def splits_for(w, sms):
-    """Smallest split count that fills one wave of CTAs (two when causal,
-    whose CTAs differ in cost); at most one split per 128-key block and 64."""
-    ctas = w.B * w.H * ((w.L + 255) // 256)
-    blocks = (w.L + 127) // 128
-    target = (2 if w.causal else 1) * sms
-    s = 1
-    while ctas * s < target and s < min(64, blocks):
-        s += 1
-    return s
+def splits_for(fa, w, sms):
+    """The library's recommended split count (``fa_splitkv_splits``): as
+    many splits as keep the CTAs within one wave (two when causal)."""
+    return fa.fa_splitkv_splits(w.B, w.H, w.L, w.d, w.causal, sms)
 
 
 # Shapes whose single-pass grid underfills the GPU (one head, long rows):
@@ -577,7 +571,7 @@ def run_ours(args):
             for name, B, H, L, d, causal in SPLITKV_SHAPES:
                 wx = AttentionWorkload(name, B, H, L, d, causal, 1.0 / math.sqrt(d), 100 + L)
                 qx, kx, vx = device_inputs(wx, dev, torch)
-                S = splits_for(wx, sms)
+                S = splits_for(fa, wx, sms)
                 steps = max(3, min(args.extra_steps, int(2e13 / wx.flops)))
                 t1 = time_forward(fa, torch, qx, kx, vx, wx, steps, 3, flush_buf)
                 t2 = time_splitkv(fa, torch, qx, kx, vx, wx, S, steps, 3, flush_buf)

@@ -29,7 +29,7 @@ __all__ = [
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED_D", "FA_ERR_MISALIGNED",
     "FA_ERR_DEVICE", "FA_ERR_LAUNCH", "FA_ERR_TIMEOUT", "FAError",
     "library", "fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_static", "FA_STATIC_WORKSPACE_BYTES",
-    "fa_splitkv_workspace_bytes", "fa_device_status",
+    "fa_splitkv_workspace_bytes", "fa_splitkv_splits", "fa_device_status",
     "fa_set_wait_timeout_ns", "fa_test_withhold_q_load", "fa_status_string", "fa_version",
     "fa_bwd", "fa_bwd_workspace_bytes", "fa_quantize_fp8", "fa_fwd_fp8",
     "fa_fwd_host", "fa_fwd_host_workspace_bytes", "forward_host",
@@ -76,6 +76,8 @@ def library() -> ctypes.CDLL:
         lib.fa_fwd_splitkv_static.restype = ci
         lib.fa_splitkv_workspace_bytes.argtypes = [ci, ci, ci, ci, ci]
         lib.fa_splitkv_workspace_bytes.restype = ctypes.c_size_t
+        lib.fa_splitkv_splits.argtypes = [ci, ci, ci, ci, ci, ci]
+        lib.fa_splitkv_splits.restype = ci
         lib.fa_device_status.argtypes = [vp, ci]
         lib.fa_device_status.restype = ci
         lib.fa_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
@@ -131,6 +133,10 @@ FA_STATIC_WORKSPACE_BYTES = 64 << 20
 
 def fa_splitkv_workspace_bytes(B, H, L, d, n_splits) -> int:
     return library().fa_splitkv_workspace_bytes(B, H, L, d, n_splits)
+
+
+def fa_splitkv_splits(B, H, L, d, causal, num_sms=0) -> int:
+    return library().fa_splitkv_splits(B, H, L, d, int(bool(causal)), num_sms)
 
 
 def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, L, d, scale, causal, workspace,
@@ -235,9 +241,10 @@ def forward(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
     return out, lse
 
 
-def forward_splitkv(q, k, v, n_splits, scale=None, causal=False, out=None, lse=None,
+def forward_splitkv(q, k, v, n_splits=None, scale=None, causal=False, out=None, lse=None,
                     workspace=None, stream=None):
-    """:func:`forward` computed in ``n_splits`` key splits plus a merge.
+    """:func:`forward` computed in ``n_splits`` key splits plus a merge
+    (``None``: the library's recommendation, ``fa_splitkv_splits``).
 
     ``workspace`` (a CUDA uint8 tensor of at least
     ``fa_splitkv_workspace_bytes(B, H, L, d, n_splits)`` bytes, 256-byte
@@ -253,6 +260,9 @@ def forward_splitkv(q, k, v, n_splits, scale=None, causal=False, out=None, lse=N
     B, H, L, d = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(d)
+    if n_splits is None:
+        with torch.cuda.device(q.device):
+            n_splits = fa_splitkv_splits(B, H, L, d, causal)
     need = fa_splitkv_workspace_bytes(B, H, L, d, n_splits)
     if need == 0:
         raise ValueError("invalid sizes or n_splits for split-KV")

@@ -354,6 +354,25 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
                 : launch<128, false, false>(p.mq, p.mk, p.mv, p.args, 1, s, p.dev);
 }
 
+int fa_splitkv_splits(int B, int H, int L, int d, int causal, int num_sms) {
+  if (B < 1 || H < 1 || L < 1 || (d != 64 && d != 128) || (causal != 0 && causal != 1))
+    return 0;
+  if (num_sms <= 0) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        num_sms <= 0)
+      return 0;
+  }
+  const int64_t ctas = static_cast<int64_t>(B) * H *
+                       ((static_cast<int64_t>(L) + fa::ROWS_PER_CTA - 1) / fa::ROWS_PER_CTA);
+  const int64_t blocks = (static_cast<int64_t>(L) + fa::BLOCK_N - 1) / fa::BLOCK_N;
+  int64_t s = static_cast<int64_t>(num_sms) * (causal ? 2 : 1) / ctas;
+  const int64_t cap = blocks < fa::kMaxSplits ? blocks : fa::kMaxSplits;
+  s = s < 1 ? 1 : (s > cap ? cap : s);
+  return static_cast<int>(s);
+}
+
 size_t fa_splitkv_workspace_bytes(int B, int H, int L, int d, int n_splits) {
   if (B < 1 || H < 1 || L < 1 || (d != 64 && d != 128) || n_splits < 1 ||
       n_splits > fa::kMaxSplits)

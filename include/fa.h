@@ -119,6 +119,25 @@ int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *
 size_t fa_splitkv_workspace_bytes(int B, int H, int L, int d, int n_splits);
 
 /*
+ * fa_splitkv_splits -- the split count this library recommends for
+ * fa_fwd_splitkv on these sizes: as many splits as fit the single-pass
+ * CTAs (one per 256 query rows of a head) into one wave over `num_sms`
+ * SMs, two waves when causal (the causal CTAs of a head differ in cost, so
+ * splitting the longest shortens the launch even past one wave), and at
+ * least 1, at most min(64, ceil(L / 128)).  A result of 1 means the
+ * single pass (fa_fwd) fills the GPU by itself.  Measured on GB300 (152
+ * SMs), one split more than this puts a few CTAs in an extra wave and
+ * costs 20-35%.
+ *
+ *   num_sms : SMs of the target GPU; <= 0 queries the current device (the
+ *             only case that makes a CUDA call).
+ *
+ * Returns 0 for invalid sizes (B/H/L < 1, d not 64/128, causal not 0/1) or
+ * when the device query fails.
+ */
+int fa_splitkv_splits(int B, int H, int L, int d, int causal, int num_sms);
+
+/*
  * FA_STATIC_WORKSPACE_BYTES -- size of the split-KV scratch array the library
  * keeps in device memory for fa_fwd_splitkv_static (64 MiB, held on every
  * GPU that loads the library until the process exits).

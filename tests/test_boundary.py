@@ -131,6 +131,25 @@ def test_splitkv_workspace_bytes(lib):
     assert fa.fa_splitkv_workspace_bytes(0, H, L, d, S) == 0
 
 
+def test_splitkv_recommended_splits(lib):
+    # as many splits as keep the single-pass CTAs (one per 256 rows of a
+    # head) within one wave of 152 SMs, two waves when causal; capped by the
+    # number of 128-key blocks and 64; host arithmetic only when the SM count
+    # is given
+    sms = 152
+    assert fa.fa_splitkv_splits(1, 1, 8192, 128, False, sms) == 4     # 32 CTAs
+    assert fa.fa_splitkv_splits(1, 1, 16384, 64, False, sms) == 2     # 64 CTAs
+    assert fa.fa_splitkv_splits(1, 1, 32768, 128, True, sms) == 2     # 128 CTAs, causal
+    assert fa.fa_splitkv_splits(2, 4, 4096, 64, False, sms) == 1      # 128 CTAs
+    assert fa.fa_splitkv_splits(1, 8, 8192, 128, True, sms) == 1      # 256 CTAs, causal
+    assert fa.fa_splitkv_splits(1, 1, 1024, 64, False, sms) == 8      # 4 CTAs: 8 key blocks
+    assert fa.fa_splitkv_splits(1, 1, 128, 64, False, sms) == 1       # one key block
+    assert fa.fa_splitkv_splits(1, 1, 100000, 64, False, 1 << 20) == 64  # the cap
+    assert fa.fa_splitkv_splits(0, 1, 128, 64, False, sms) == 0
+    assert fa.fa_splitkv_splits(1, 1, 128, 96, False, sms) == 0
+    assert lib.fa_splitkv_splits(1, 1, 128, 64, 2, sms) == 0
+
+
 def _call_split(ws=0x1000000, ws_bytes=None, n_splits=4, **over):
     a = dict(GOOD)
     a.update(over)

@@ -123,3 +123,19 @@ def test_splitkv_back_to_back_calls_share_one_workspace(dev):
         o_ref, lse_ref, a_ref = oracle_forward(_f64(qb), _f64(kb), _f64(vb), 0.125, False)
         check_parity(from_device(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
                      "back to back", absv_ref=a_ref)
+
+
+def test_splitkv_recommended_split_count(dev):
+    # n_splits=None takes the library's recommendation for the current GPU
+    import torch
+    L, d = 3000, 128
+    qb, kb, vb = make_custom(1, 1, L, d, seed=41)
+    S = fa.fa_splitkv_splits(1, 1, L, d, True)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    assert S == fa.fa_splitkv_splits(1, 1, L, d, True, sms) and S > 1
+    q, k, v = (to_device(x, dev) for x in (qb, kb, vb))
+    o, lse = fa.forward_splitkv(q, k, v, scale=0.09, causal=True)
+    torch.cuda.synchronize()
+    o_ref, lse_ref, a_ref = oracle_forward(_f64(qb), _f64(kb), _f64(vb), 0.09, True)
+    check_parity(from_device(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
+                 "recommended splits", absv_ref=a_ref)
