@@ -129,8 +129,8 @@ struct BwdCfg {
   static constexpr int DS_OFF = STAGE_OFF + STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = DS_OFF + BWD_DS_BYTES;
   // kv_full, fullQ[S], fulldO[S], dq_staged[S], s_full, dp_full, p_ready,
-  // ds_ready, dq_full, dq_free, drain, dq_full2, dq_staged2[S]
-  static constexpr int NBAR = 1 + 3 * STAGES + 7 + 1 + STAGES;
+  // ds_ready, dq_full, dq_free, drain, dq_full2, dq_staged2[S], fin
+  static constexpr int NBAR = 1 + 3 * STAGES + 7 + 1 + STAGES + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   // The tiles need a 1024-byte aligned base; the launch adds as much slack
   // as the 227 KB budget leaves (up to 1024 bytes) and the kernel checks the
@@ -395,6 +395,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   const uint32_t bar_dq2 = bar_s + 56;  // second half of dQ_i (DQ_HALVES)
   // dq_staged2 of stage s: the second half of the stage's dQ (DQ_HALVES)
   auto bar_dqst2 = [&](int s) { return bar_s + 64 + 8u * s; };
+  // every MMA of the CTA has completed (one commit after the last block)
+  const uint32_t bar_fin = bar_s + 64 + 8u * C::STAGES;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + C::MISC_OFF);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::MISC_OFF + 4);
 
@@ -434,6 +436,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(bar_dqfree, C::DQ_COPIERS);
     mbar_init(bar_drain, 1);
     mbar_init(bar_dq2, 1);
+    mbar_init(bar_fin, 1);
     for (int s = 0; s < C::STAGES; ++s) mbar_init(bar_dqst2(s), C::DQ_COPIERS);
     *abort_flag = 0;
     fence_mbarrier_init();
@@ -682,6 +685,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         if (!ok) break;
       }
     }
+    if (ok) {
+      if (elect_one()) mma_commit(bar_fin);
+      __syncwarp();
+    }
     if (!ok) {
       // Every MMA already issued must finish before the tensor memory is freed.
       if (elect_one()) {
@@ -919,11 +926,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       }
     }
 
-    // Epilogue: the last dq_full arrival came after every MMA of the CTA, so
-    // dV_j and dK_j are final (the gradient warps wait for it here when the
-    // dQ warps copy dQ out).  bf16 (round to nearest even), rows < L.
+    // Epilogue: dV_j and dK_j are final once every MMA of the CTA has
+    // completed.  With phase C on these warps the last dq_full arrival says
+    // so; when the dQ warps copy dQ out, these warps wait for the MMA warp's
+    // final commit instead (a single phase: they observe none of dq_full's,
+    // and a parity wait on a barrier several phases behind would alias).
+    // bf16 (round to nearest even), rows < L.
     if (C::DQ_WARPS > 0 && ok) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_dq, (n_i - 1) & 1, ctl, SITE_B_DQ));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_fin, 0, ctl, SITE_B_DQ));
       if (ok) tc_fence_after();
     }
     if (ok) {
