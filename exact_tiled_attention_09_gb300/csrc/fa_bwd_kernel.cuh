@@ -30,7 +30,7 @@
 // reduce-adds; every key block of the head contributes to every dQ_i).
 // Post-pass: dQ = bf16(accumulator).
 //
-// Warp roles (576 threads):
+// Warp roles (576 threads; 704 at d = 64):
 //   warp 0      MMA issuer, owner of the tensor memory (whole warp polls,
 //               one elected lane issues)
 //   warp 1      TMA producer: K_j, V_j once; Q_i and dO_i into a ring of
@@ -38,6 +38,8 @@
 //               reduce-adds
 //   warps 2..17 gradient warps: warp w handles TMEM lanes 32*(w%4)..+31
 //               (its keys) and query columns 32*h..32*h+31, h = (w-2)/4
+//   warps 18..21 d = 64 only: dQ warps, one per TMEM lane quarter: copy dQ_i
+//               out of tensor memory and stage it (phase C below)
 //
 // Tensor memory (512 columns): [0,128) S^T, then P^T as packed bf16 (group
 // h's 32 queries in columns 32h..32h+15); [128,256) dP^T, then dQ_i
@@ -50,12 +52,14 @@
 //            column halves) | S_{i+1}
 //   d = 64:  dP_i | wait P ready: dV_i, S_{i+1} | wait dS ready: dK_i, dQ_i
 // and the gradient warps work on phases A (P), B (dS), C (dQ out) as
-// A(i) B(i) C(i) at d = 128 and A(0), then B(i) A(i+1) C(i) at d = 64, where
-// the MMA work per block is half as large and P of the next block is
-// computed while dK_i and dQ_i run.  S_{i+1} overwrites P^T_i only after dV_i
-// has read it; dP_{i+1} waits until the gradient warps have copied dQ_i out
-// of its columns, so its commit also proves dK_i and dQ_i have read the dS
-// tile before the gradient warps write dS_{i+1}.
+// A(i) B(i) C(i) at d = 128 and A(0), then B(i) A(i+1) at d = 64, where the
+// MMA work per block is half as large, P of the next block is computed
+// while dK_i and dQ_i run, and the dQ warps run C(i).  S_{i+1} overwrites
+// P^T_i only after dV_i has read it; dP_{i+1} is issued after dK_i and dQ_i
+// (at d = 128 also after dQ_i has left its columns), so its commit proves
+// dK_i and dQ_i have read the dS tile before the gradient warps write
+// dS_{i+1}.  After the last block the MMA warp commits once more (fin): the
+// epilogue's wait when the dQ warps, not the gradient warps, track dq_full.
 //
 // Copies and the dQ path.  Q_i (with its per-query terms) and dO_i have
 // separate full barriers.  dQ_i leaves through the producer warp: the
