@@ -113,6 +113,20 @@ bool configure_once(Kernel kernel, int smem, int dev, bool* configured, std::mut
   return true;
 }
 
+// Multiprocessor count of device `dev`, queried once (0 if the query fails).
+int sm_count(int dev) {
+  static int count[kMaxDevices] = {};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 0 || dev >= kMaxDevices) return 0;
+  if (count[dev] <= 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    count[dev] = n;
+  }
+  return count[dev];
+}
+
 template <int D, bool CAUSAL, bool SPLIT, bool FP8 = false>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
            const FwdArgs& args, int n_splits, cudaStream_t stream, int dev) {
@@ -256,7 +270,7 @@ size_t workspace_bytes(int64_t BH, int L, int d, int n_splits) {
 // per-query terms -lse*log2(e) and -scale*<dO_i, O_i>, each [BH, Lp] with
 // Lp = L rounded up to 128, every part 256-byte aligned.
 struct BwdLayout {
-  size_t acc_bytes, row_bytes, total;
+  size_t acc_bytes, row_bytes, total;  // the unit counter sits in the last 256 bytes
 };
 
 BwdLayout bwd_layout(int64_t BH, int L, int d) {
@@ -264,7 +278,7 @@ BwdLayout bwd_layout(int64_t BH, int L, int d) {
   BwdLayout w;
   w.acc_bytes = align256(static_cast<size_t>(BH) * static_cast<size_t>(L) * d * 4);
   w.row_bytes = align256(static_cast<size_t>(BH) * Lp * 4);
-  w.total = w.acc_bytes + 2 * w.row_bytes;
+  w.total = w.acc_bytes + 2 * w.row_bytes + 256;
   return w;
 }
 
@@ -284,8 +298,12 @@ int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   // The gradient kernel and the post-pass are programmatic dependants of the
   // kernel before them: each starts while that one drains and waits for it
-  // before reading its results.
-  const dim3 grid(static_cast<unsigned>(args.bh) * static_cast<unsigned>(args.n_kv));
+  // before reading its results.  The gradient kernel is persistent: one CTA
+  // per SM (its shared memory admits no second), each taking units until
+  // none is left.
+  const int sms = sm_count(dev);
+  if (sms <= 0) return FA_ERR_DEVICE;
+  const dim3 grid(static_cast<unsigned>(args.n_units < sms ? args.n_units : sms));
   if (launch_dependent(kernel, grid, dim3(BwdCfg<D>::THREADS), smem, stream, mq, mk, mv, mdo, mdq,
                        args) != cudaSuccess)
     return FA_ERR_LAUNCH;
@@ -481,6 +499,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   if (!encode_map_f32_acc(&mdq, acc, static_cast<int>(BH), L, d)) return FA_ERR_LAUNCH;
   float* nlse2 = reinterpret_cast<float*>(ws + w.acc_bytes);
   float* nds = reinterpret_cast<float*>(ws + w.acc_bytes + w.row_bytes);
+  unsigned int* sched = reinterpret_cast<unsigned int*>(ws + w.acc_bytes + 2 * w.row_bytes);
   const int Lp = static_cast<int>(n_kv * 128);
 
   BwdArgs args;
@@ -493,6 +512,8 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   args.Lp = Lp;
   args.n_kv = static_cast<int>(n_kv);
   args.bh = static_cast<int>(BH);
+  args.n_units = static_cast<int>(BH * n_kv);
+  args.sched = sched;
   {
     // Heads per scheduling group: Q + dO (bf16) and the fp32 dQ accumulator
     // of a group within ~32 MB of L2.
@@ -513,6 +534,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   pre.nlse2 = nlse2;
   pre.nds = nds;
   pre.dq_acc = acc;
+  pre.sched = sched;
   pre.L = L;
   pre.Lp = Lp;
   pre.rows = BH * Lp;

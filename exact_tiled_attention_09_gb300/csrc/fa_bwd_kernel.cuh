@@ -10,11 +10,15 @@
 // The row sum rowsum(dP (.) P)_i equals <dO_i, O_i> (dP = dO V^T and O = P V),
 // which a pre-pass computes once per query row from O and dO.
 //
-// Work unit: one CTA owns one block of 128 keys of one (batch, head), keeps
+// Work unit: one block j of 128 keys of one (batch, head).  Its CTA keeps
 // K_j and V_j in shared memory and dK_j, dV_j in tensor memory, and walks
-// the query blocks i (all of them, or i >= j with the causal mask).  Per
-// query block it computes, transposed so that its own keys are the TMEM
-// lanes:
+// the query blocks i (all of them, or i >= j with the causal mask).  The
+// grid is persistent, one CTA per SM: a CTA starts with the unit of its
+// own index and then claims the next unclaimed unit from a counter (zeroed
+// by the pre-pass), so the set-up, the tensor-memory allocation and the
+// launch of a CTA are paid once per SM, and the next unit's first copies
+// and products start while the last one's dK and dV leave.  Per query block
+// a unit computes, transposed so that its own keys are the TMEM lanes:
 //
 //   S^T  = K_j Q_i^T                (SS MMA, M = keys, N = queries, K = d)
 //   dP^T = V_j dO_i^T               (SS MMA)
@@ -33,9 +37,11 @@
 // Warp roles (576 threads; 704 at d = 64):
 //   warp 0      MMA issuer, owner of the tensor memory (whole warp polls,
 //               one elected lane issues)
-//   warp 1      TMA producer: K_j, V_j once; Q_i and dO_i into a ring of
-//               stages (two at d = 128, three at d = 64); issues the dQ
-//               reduce-adds
+//   warp 1      TMA producer: K_j, V_j per unit; Q_i and dO_i into a ring
+//               of stages (two at d = 128, three at d = 64), continued
+//               across units; issues the dQ reduce-adds; claims units and
+//               publishes each in one of two shared-memory slots (full /
+//               free barriers) that the other roles read
 //   warps 2..17 gradient warps: warp w handles TMEM lanes 32*(w%4)..+31
 //               (its keys) and query columns 32*h..32*h+31, h = (w-2)/4
 //   warps 18..21 d = 64 only: dQ warps, one per TMEM lane quarter: copy dQ_i
@@ -58,8 +64,14 @@
 // P^T_i only after dV_i has read it; dP_{i+1} is issued after dK_i and dQ_i
 // (at d = 128 also after dQ_i has left its columns), so its commit proves
 // dK_i and dQ_i have read the dS tile before the gradient warps write
-// dS_{i+1}.  After the last block the MMA warp commits once more (fin): the
-// epilogue's wait when the dQ warps, not the gradient warps, track dq_full.
+// dS_{i+1}.  After a unit's last block the MMA warp commits once more
+// (fin): the producer waits for it before copying the next unit's K and V
+// over the last ones, and so does the epilogue when the dQ warps, not the
+// gradient warps, track dq_full.  Blocks are numbered across the CTA's
+// units, so each once-per-block barrier simply continues its phases from
+// one unit to the next; the next unit's dV and dK products (which start
+// their accumulators afresh) wait for its first P, which the gradient warps
+// write only after reading the previous dV and dK out.
 //
 // Copies and the dQ path.  Q_i (with its per-query terms) and dO_i have
 // separate full barriers.  dQ_i leaves through the producer warp: the
@@ -109,6 +121,8 @@ enum : uint32_t {
   SITE_B_DQ = 15,
   SITE_B_DQFREE = 16,
   SITE_B_ALIGN = 17,  // not a wait: the shared-memory base left too little slack
+  SITE_B_UNIT = 18,   // a unit slot (published or taken by every reader)
+  SITE_B_FIN = 19,    // the producer's wait for the previous unit's MMAs
 };
 
 template <int D>
@@ -133,13 +147,16 @@ struct BwdCfg {
   static constexpr int DS_OFF = STAGE_OFF + STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = DS_OFF + BWD_DS_BYTES;
   // kv_full, fullQ[S], fulldO[S], dq_staged[S], s_full, dp_full, p_ready,
-  // ds_ready, dq_full, dq_free, drain, dq_full2, dq_staged2[S], fin
-  static constexpr int NBAR = 1 + 3 * STAGES + 7 + 1 + STAGES + 1;
+  // ds_ready, dq_full, dq_free, drain, dq_full2, dq_staged2[S], fin,
+  // unit_full[2], unit_free[2]
+  static constexpr int NBAR = 1 + 3 * STAGES + 7 + 1 + STAGES + 1 + 4;
+  // then the TMEM address, the abort flag and the two unit slots (unit
+  // index and its query-block count, 8 B each)
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   // The tiles need a 1024-byte aligned base; the launch adds as much slack
   // as the 227 KB budget leaves (up to 1024 bytes) and the kernel checks the
   // slack it actually needs.
-  static constexpr int USED_BYTES = MISC_OFF + 16;
+  static constexpr int USED_BYTES = MISC_OFF + 24;
   static constexpr int SLACK = (232448 - USED_BYTES) < 1024 ? (232448 - USED_BYTES) / 16 * 16 : 1024;
   static constexpr int SMEM_BYTES = USED_BYTES + SLACK;
   static_assert(SLACK >= 0 && SMEM_BYTES <= 232448, "shared memory budget");
@@ -175,6 +192,8 @@ struct BwdCfg {
   static constexpr int THREADS = 32 * (FIRST_DQ_WARP + DQ_WARPS);
   // arrivals on dq_free and dq_staged: the warps that copy dQ out
   static constexpr int DQ_COPIERS = DQ_WARPS ? DQ_WARPS : BWD_GRAD_WARPS;
+  // warps that read every published unit: the MMA, gradient and dQ warps
+  static constexpr int UNIT_READERS = 1 + BWD_GRAD_WARPS + DQ_WARPS;
   static constexpr uint32_t DQ_COL = SPLIT_DQ ? 256 + 2 * D : DP_COL;
   static_assert(!SPLIT_DQ || DQ_COL + D <= 512, "tensor memory budget");
 };
@@ -194,7 +213,9 @@ struct BwdArgs {
   float scale;
   unsigned int* status;
   unsigned long long timeout_ns;
-  int test_withhold_kv;    // test hook: skip the K/V copy so the first wait runs out
+  int test_withhold_kv;    // test hook: skip the K/V copies so the first wait runs out
+  unsigned int* sched;     // units claimed after the first wave, zeroed by the pre-pass
+  int n_units;             // B * H * n_kv
 };
 
 // Pre-pass arguments: per query row, the two per-row terms the main kernel
@@ -206,6 +227,7 @@ struct BwdPreArgs {
   float* nlse2;            // fp32 [BH, Lp]
   float* nds;              // fp32 [BH, Lp]
   float* dq_acc;           // fp32 [BH, L, D]
+  unsigned int* sched;     // the main kernel's unit counter
   int L;
   int Lp;
   long long rows;          // BH * Lp
@@ -257,9 +279,10 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // Pre-pass, one warp per BWD_PRE_ROWS consecutive rows of [BH, Lp]:
 // D_i = <dO_i, O_i> (fp32, bf16 inputs), stored as -scale * D_i, and
 // -lse_i * log2(e); rows past L get the values that make them vanish in the
-// main kernel (P = 0, dS = 0).  It also zeroes the dQ accumulator rows.  The
-// loads of all the warp's rows are issued before any is used (more bytes in
-// flight per warp: the kernel is bound by HBM).  The main kernel is its
+// main kernel (P = 0, dS = 0).  It also zeroes the dQ accumulator rows, and
+// block 0 the main kernel's unit counter.  The loads of all the warp's rows
+// are issued before any is used (more bytes in flight per warp: the kernel
+// is bound by HBM).  The main kernel is its
 // programmatic dependant: it is launched as the last blocks of this grid
 // exit (no early trigger: a gradient CTA resident early would take the
 // registers that blocks of this pass need on its SM).
@@ -269,6 +292,7 @@ __global__ void __launch_bounds__(BWD_AUX_WARPS * 32) fa_bwd_pre_kernel(const Bw
   const long long row0 =
       (static_cast<long long>(blockIdx.x) * BWD_AUX_WARPS + (threadIdx.x >> 5)) * BWD_PRE_ROWS;
   const int lane = threadIdx.x & 31;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *a.sched = 0u;
   Vec ow[BWD_PRE_ROWS], dw[BWD_PRE_ROWS];
   bool live[BWD_PRE_ROWS];
 #pragma unroll
@@ -347,7 +371,8 @@ __global__ void __launch_bounds__(256) fa_bwd_post_kernel(const float* __restric
   }
 }
 
-// Main backward kernel: one CTA per (head, key block); see the file comment.
+// Main backward kernel: persistent, one CTA per SM, each taking work units
+// (head, key block) in turn; see the file comment.
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -399,31 +424,45 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   const uint32_t bar_dq2 = bar_s + 56;  // second half of dQ_i (DQ_HALVES)
   // dq_staged2 of stage s: the second half of the stage's dQ (DQ_HALVES)
   auto bar_dqst2 = [&](int s) { return bar_s + 64 + 8u * s; };
-  // every MMA of the CTA has completed (one commit after the last block)
+  // every MMA of the current unit has completed (one commit after its last
+  // block)
   const uint32_t bar_fin = bar_s + 64 + 8u * C::STAGES;
+  // unit slot s: written by the producer (unit_full), read by every reader
+  // warp (unit_free)
+  auto bar_ufull = [&](int s) { return bar_fin + 8u + 8u * s; };
+  auto bar_ufree = [&](int s) { return bar_fin + 24u + 8u * s; };
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + C::MISC_OFF);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::MISC_OFF + 4);
+  volatile int* const unit_slot = reinterpret_cast<volatile int*>(base_ptr + C::MISC_OFF + 8);
 
   const int warp = warp_index_uniform();
   const int lane = threadIdx.x & 31;
   const int L = args.L;
   const int n_kv = args.n_kv;
 
-  // CTA order.  Heads go in groups of `group_heads` whose Q, dO and dQ
-  // accumulator fit comfortably in L2 (every key block of a head re-reads
-  // them).  Non-causal CTAs all cost the same and go head-major; causal key
-  // block j visits n_kv - j query blocks, so within a group block 0 of every
-  // head goes first (longest first).
-  const int BH = args.bh;
-  const int G = args.group_heads;
-  const int idx = static_cast<int>(blockIdx.x);
-  const int g0 = (idx / (G * n_kv)) * G;
-  const int gsz = min(G, BH - g0);
-  const int rk = idx - g0 * n_kv;
-  const int bh = CAUSAL ? g0 + rk % gsz : g0 + rk / n_kv;
-  const int jblk = CAUSAL ? rk / gsz : rk % n_kv;
-  const int q_first = CAUSAL ? jblk : 0;
-  const int n_i = n_kv - q_first;  // query blocks visited, >= 1
+  // Work units in claim order.  Heads go in groups of `group_heads` whose Q,
+  // dO and dQ accumulator fit comfortably in L2 (every key block of a head
+  // re-reads them).  Non-causal units all cost the same and go head-major;
+  // causal key block j visits n_kv - j query blocks, so within a group block
+  // 0 of every head goes first (longest first).  A CTA starts with unit
+  // blockIdx.x and then claims the next unclaimed one from a counter in the
+  // workspace, as the hardware would hand out CTAs.
+  struct Unit {
+    int bh, jblk, q_first, n_i;
+  };
+  auto decode = [&](int idx) {
+    const int BH = args.bh;
+    const int G = args.group_heads;
+    const int g0 = (idx / (G * n_kv)) * G;
+    const int gsz = min(G, BH - g0);
+    const int rk = idx - g0 * n_kv;
+    Unit u;
+    u.bh = CAUSAL ? g0 + rk % gsz : g0 + rk / n_kv;
+    u.jblk = CAUSAL ? rk / gsz : rk % n_kv;
+    u.q_first = CAUSAL ? u.jblk : 0;
+    u.n_i = n_kv - u.q_first;  // query blocks visited, >= 1
+    return u;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(bar_kv, 1);
@@ -442,6 +481,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(bar_dq2, 1);
     mbar_init(bar_fin, 1);
     for (int s = 0; s < C::STAGES; ++s) mbar_init(bar_dqst2(s), C::DQ_COPIERS);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar_ufull(s), 1);
+      mbar_init(bar_ufree(s), C::UNIT_READERS);
+    }
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -465,62 +508,117 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const bool w = mbar_wait(bar, parity, ctl, site);
     return __all_sync(0xffffffffu, w);
   };
-  auto use_parity = [](int blk) { return static_cast<uint32_t>(blk / C::STAGES) & 1u; };
+  // Blocks are counted over all the CTA's units: block b uses stage
+  // b % STAGES, the stage's (b / STAGES)-th phase, and phase b of each
+  // once-per-block barrier.  All three depend on b modulo BM = 2 * STAGES
+  // only, which is what every role keeps (no overflow however many units a
+  // CTA takes).
+  constexpr int BM = 2 * C::STAGES;
+  auto stage_of = [](int b) { return b % C::STAGES; };
+  auto use_parity = [](int b) { return static_cast<uint32_t>(b / C::STAGES) & 1u; };
+  auto par = [](int b) { return static_cast<uint32_t>(b) & 1u; };
+  // Unit k of this CTA (k = 0, 1, ...), for a reader warp: its index (and
+  // its query-block count in n_i), -1 after the last one, or -2 if the wait
+  // gave up.
+  auto read_unit = [&](int k, int& n_i) -> int {
+    const int s = k & 1;
+    if (!warp_wait(bar_ufull(s), static_cast<uint32_t>(k >> 1) & 1u, SITE_B_UNIT)) return -2;
+    const int u = unit_slot[2 * s];
+    n_i = unit_slot[2 * s + 1];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_ufree(s));
+    return u;
+  };
 
   if (warp == 1) {
     // ------------------------------------------------------------ producer
-    if (!args.test_withhold_kv && elect_one()) {
-      mbar_arrive_expect_tx(bar_kv, 2 * C::TILE_BYTES);
-      for (int c = 0; c < C::BOXES; ++c) {
-        tma_load_3d(sK + c * BOX, &tmK, bar_kv, c * 64, jblk * 128, bh);
-        tma_load_3d(sV + c * BOX, &tmV, bar_kv, c * 64, jblk * 128, bh);
-      }
+    Unit u = decode(static_cast<int>(blockIdx.x));
+    if (lane == 0) {
+      unit_slot[0] = static_cast<int>(blockIdx.x);
+      unit_slot[1] = u.n_i;
+      mbar_arrive(bar_ufull(0));
     }
     __syncwarp();
-    // The per-query terms and the zeroed dQ accumulator come from the
-    // pre-pass, which may still be running (programmatic launch).
+    auto load_kv = [&](const Unit& w) {
+      if (!args.test_withhold_kv && elect_one()) {
+        mbar_arrive_expect_tx(bar_kv, 2 * C::TILE_BYTES);
+        for (int c = 0; c < C::BOXES; ++c) {
+          tma_load_3d(sK + c * BOX, &tmK, bar_kv, c * 64, w.jblk * 128, w.bh);
+          tma_load_3d(sV + c * BOX, &tmV, bar_kv, c * 64, w.jblk * 128, w.bh);
+        }
+      }
+      __syncwarp();
+    };
+    load_kv(u);
+    uint32_t kv_par = 0;  // phase parity of the last K/V load
+    // The per-query terms, the zeroed dQ accumulator and the zeroed unit
+    // counter come from the pre-pass, which may still be running
+    // (programmatic launch).
     pdl_wait();
-    auto load_q = [&](int blk) {
-      const int st = blk % C::STAGES;
+    // (head, query block) of the block each stage holds, for its reduce
+    int st_bh[C::STAGES], st_qb[C::STAGES];
+#pragma unroll
+    for (int t = 0; t < C::STAGES; ++t) st_bh[t] = st_qb[t] = 0;
+    // per stage: loaded at all (bit s), the phase parity of its last Q / dO
+    // load (for the drain after an abort)
+    uint32_t q_used = 0, q_par = 0, do_used = 0, do_par = 0;
+    auto load_q = [&](int blk, int b, int qb) {
+      const int st = stage_of(blk);
+      q_used |= 1u << st;
+      q_par = (q_par & ~(1u << st)) | (use_parity(blk) << st);
       if (elect_one()) {
         mbar_arrive_expect_tx(bar_fullq(st), C::TILE_BYTES + 1024);
-        const int row = (q_first + blk) * 128;
+        const int row = qb * 128;
         for (int c = 0; c < C::BOXES; ++c)
-          tma_load_3d(sQ(st) + c * BOX, &tmQ, bar_fullq(st), c * 64, row, bh);
-        const size_t term = static_cast<size_t>(bh) * args.Lp + row;
+          tma_load_3d(sQ(st) + c * BOX, &tmQ, bar_fullq(st), c * 64, row, b);
+        const size_t term = static_cast<size_t>(b) * args.Lp + row;
         const uint32_t terms = smem_u32(rowterms(st));
         bulk_load_1d(terms, args.nlse2 + term, 512, bar_fullq(st));
         bulk_load_1d(terms + 512, args.nds + term, 512, bar_fullq(st));
       }
       __syncwarp();
     };
-    auto load_do = [&](int blk) {
-      const int st = blk % C::STAGES;
+    auto load_do = [&](int blk, int b, int qb) {
+      const int st = stage_of(blk);
+      do_used |= 1u << st;
+      do_par = (do_par & ~(1u << st)) | (use_parity(blk) << st);
       if (elect_one()) {
         mbar_arrive_expect_tx(bar_fulldo(st), C::TILE_BYTES);
-        const int row = (q_first + blk) * 128;
         for (int c = 0; c < C::BOXES; ++c)
-          tma_load_3d(sdO(st) + c * BOX, &tmdO, bar_fulldo(st), c * 64, row, bh);
+          tma_load_3d(sdO(st) + c * BOX, &tmdO, bar_fulldo(st), c * 64, qb * 128, b);
       }
       __syncwarp();
+#pragma unroll
+      for (int t = 0; t < C::STAGES; ++t)
+        if (t == st) {
+          st_bh[t] = b;
+          st_qb[t] = qb;
+        }
     };
     // dQ of block blk is staged: add it into the accumulator (one reduce per
     // box, 32 rows x 32 floats each) in two groups, the boxes in the Q
     // buffer first.  Returns once the Q buffer has been read; the caller
     // waits for the rest (bulk_wait_group_read0) before reusing the dO
-    // buffer.
+    // buffer.  The stage's coordinates are those of blk until load_do
+    // refills it.
     auto reduce_half = [&](int blk, int half) {
-      const int st = blk % C::STAGES;
+      const int st = stage_of(blk);
+      int b = 0, qb = 0;
+#pragma unroll
+      for (int t = 0; t < C::STAGES; ++t)
+        if (t == st) {
+          b = st_bh[t];
+          qb = st_qb[t];
+        }
       if (elect_one()) {
-        const int qb = q_first + blk;
         for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c)
-          tma_reduce_add_3d(&tmdQ, dq_box(st, 4 * c), 32 * c, qb * 128, bh);
+          tma_reduce_add_3d(&tmdQ, dq_box(st, 4 * c), 32 * c, qb * 128, b);
         bulk_commit_group();
       }
       __syncwarp();
     };
     auto reduce_block = [&](int blk) -> bool {
-      const int st = blk % C::STAGES;
+      const int st = stage_of(blk);
       if (!warp_wait(bar_dqst(st), use_parity(blk), SITE_B_DQST)) return false;
       reduce_half(blk, 0);
       if (C::DQ_HALVES && !warp_wait(bar_dqst2(st), use_parity(blk), SITE_B_DQST)) return false;
@@ -529,58 +627,98 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       __syncwarp();
       return true;
     };
-    // Block k reuses the stage of block k - STAGES: Q_k once the first reduce
-    // group of that block has been read, dO_k once the second has.  At d = 128 the
-    // second group is issued only after the Q_k copy (measured: Q_k arrives
-    // sooner and the wait for S_k shrinks; at d = 64 the other order is
-    // faster).
-    int q_loads = 0, do_loads = 0, reduced = 0;
+    // Block g reuses the stage of block g - STAGES: Q_g once the first reduce
+    // group of that block has been read, dO_g once the second has.  At d = 128 the
+    // second group is issued only after the Q_g copy (measured: Q_g arrives
+    // sooner and the wait for S_g shrinks; at d = 64 the other order is
+    // faster).  The K/V copy of a unit after the first follows the Q and dO
+    // copies of its first block, once every MMA of the previous unit (the
+    // last readers of K and V) has completed.
+    // Blocks modulo BM: the next to load and the next to reduce; pending
+    // blocks are loaded and not yet reduced (at most STAGES).
+    int gm = 0, rm = 0, pending = 0;
     bool ok = true;
-    for (int k = 0; k < n_i && ok; ++k) {
-      if (k >= C::STAGES) {
-        if constexpr (C::DQ_HALVES) {
-          // the first half's reduce, then Q_k into the Q buffer it frees,
-          // ahead of the second half's reduce in the copy engine
-          ok = warp_wait(bar_dqst(reduced % C::STAGES), use_parity(reduced), SITE_B_DQST);
-          if (!ok) break;
-          reduce_half(reduced, 0);
+    for (int k = 0;;) {
+      for (int i = 0; i < u.n_i && ok; ++i) {
+        const int qb = u.q_first + i;
+        const bool reuse = pending == C::STAGES;  // the stage holds block rm
+        if (reuse) {
+          if constexpr (C::DQ_HALVES) {
+            // the first half's reduce, then Q into the Q buffer it frees,
+            // ahead of the second half's reduce in the copy engine
+            ok = warp_wait(bar_dqst(stage_of(rm)), use_parity(rm), SITE_B_DQST);
+            if (!ok) break;
+            reduce_half(rm, 0);
+            if (elect_one()) bulk_wait_group_read0();
+            __syncwarp();
+          } else {
+            ok = reduce_block(rm);
+            if (!ok) break;
+            rm = (rm + 1) % BM;
+            --pending;
+          }
+        }
+        load_q(gm, u.bh, qb);
+        if (reuse) {
+          if constexpr (C::DQ_HALVES) {
+            ok = warp_wait(bar_dqst2(stage_of(rm)), use_parity(rm), SITE_B_DQST);
+            if (!ok) break;
+            reduce_half(rm, 1);
+            rm = (rm + 1) % BM;
+            --pending;
+          }
           if (elect_one()) bulk_wait_group_read0();
           __syncwarp();
-        } else {
-          ok = reduce_block(reduced);
+        }
+        load_do(gm, u.bh, qb);
+        ++pending;
+        gm = (gm + 1) % BM;
+        if (i == 0 && k > 0) {
+          ok = warp_wait(bar_fin, static_cast<uint32_t>(k - 1) & 1u, SITE_B_FIN);
           if (!ok) break;
-          ++reduced;
+          load_kv(u);
+          kv_par ^= 1u;
         }
       }
-      load_q(k);
-      ++q_loads;
-      if (k >= C::STAGES) {
-        if constexpr (C::DQ_HALVES) {
-          ok = warp_wait(bar_dqst2(reduced % C::STAGES), use_parity(reduced), SITE_B_DQST);
-          if (!ok) break;
-          reduce_half(reduced, 1);
-          ++reduced;
-        }
-        if (elect_one()) bulk_wait_group_read0();
-        __syncwarp();
+      if (!ok) break;
+      // Claim the next unit and publish it (or the end, -1) in slot k % 2
+      // once every reader has taken the unit that slot held.
+      int next = -1;
+      if (lane == 0) {
+        const long long t = static_cast<long long>(gridDim.x) + atomicAdd(args.sched, 1u);
+        next = t < args.n_units ? static_cast<int>(t) : -1;
       }
-      load_do(k);
-      ++do_loads;
+      next = __shfl_sync(0xffffffffu, next, 0);
+      if (next >= 0) {
+        u = decode(next);
+      }
+      ++k;
+      if (k >= 2) {
+        ok = warp_wait(bar_ufree(k & 1), static_cast<uint32_t>((k >> 1) - 1) & 1u, SITE_B_UNIT);
+        if (!ok) break;
+      }
+      if (lane == 0) {
+        unit_slot[2 * (k & 1)] = next;
+        unit_slot[2 * (k & 1) + 1] = next >= 0 ? u.n_i : 0;
+        mbar_arrive(bar_ufull(k & 1));
+      }
+      __syncwarp();
+      if (next < 0) break;
     }
-    for (; ok && reduced < n_i; ++reduced) ok = reduce_block(reduced);
+    for (; ok && pending > 0; --pending, rm = (rm + 1) % BM) ok = reduce_block(rm);
     if (elect_one()) {
       if (!ok) {
         // Let every copy already issued land before the CTA exits.
-        if (!args.test_withhold_kv) mbar_wait_drain(bar_kv, 0, args.timeout_ns);
+        if (!args.test_withhold_kv) mbar_wait_drain(bar_kv, kv_par, args.timeout_ns);
         for (int s = 0; s < C::STAGES; ++s) {
-          const int nq = q_loads > s ? (q_loads - 1 - s) / C::STAGES + 1 : 0;
-          const int nd = do_loads > s ? (do_loads - 1 - s) / C::STAGES + 1 : 0;
-          if (nq > 0) mbar_wait_drain(bar_fullq(s), (nq - 1) & 1, args.timeout_ns);
-          if (nd > 0) mbar_wait_drain(bar_fulldo(s), (nd - 1) & 1, args.timeout_ns);
+          if ((q_used >> s) & 1u) mbar_wait_drain(bar_fullq(s), (q_par >> s) & 1u, args.timeout_ns);
+          if ((do_used >> s) & 1u) mbar_wait_drain(bar_fulldo(s), (do_par >> s) & 1u, args.timeout_ns);
         }
       }
-      // The CTA's shared memory must outlive the reduces.
-      bulk_wait_group0();
+      // The reduces must have read the staged dQ before the shared memory
+      // goes; their writes complete with the grid, before the dependent
+      // conversion pass reads the accumulator.
+      bulk_wait_group_read0();
     }
     __syncwarp();
   } else if (warp == 0) {
@@ -607,91 +745,102 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       __syncwarp();
     };
     auto issue_next_s = [&](int blk) -> bool {
-      const int st2 = blk % C::STAGES;
+      const int st2 = stage_of(blk);
       if (!warp_wait(bar_fullq(st2), use_parity(blk), SITE_B_FULL)) return false;
       tc_fence_after();
       issue_kmajor(C::S_COL, sK, sQ(st2), bar_s);
       return true;
     };
-    bool ok = warp_wait(bar_kv, 0, SITE_B_KV);
-    if (ok) ok = warp_wait(bar_fullq(0), 0, SITE_B_FULL);
-    if (ok) {
-      tc_fence_after();
-      issue_kmajor(C::S_COL, sK, sQ(0), bar_s);
-    }
-    for (int i = 0; i < n_i && ok; ++i) {
-      const int st = i % C::STAGES;
-      if (i > 0 && !C::SPLIT_DQ) {
-        // dP_i goes into the columns dQ_{i-1} occupies until copied out
-        ok = warp_wait(bar_dqfree, (i - 1) & 1, SITE_B_DQFREE);
+    bool ok = true;
+    int g = 0;  // first block of the current unit, modulo BM
+    for (int k = 0; ok; ++k) {
+      int n_i = 0;
+      const int unit = read_unit(k, n_i);
+      if (unit < 0) {
+        ok = unit == -1;
+        break;
+      }
+      // K_j, V_j of this unit, then S of its first block
+      ok = warp_wait(bar_kv, static_cast<uint32_t>(k) & 1u, SITE_B_KV);
+      if (ok) ok = issue_next_s(g);
+      for (int i = 0; i < n_i && ok; ++i) {
+        const int b = (g + i) % BM;
+        const int st = stage_of(b);
+        if ((k > 0 || i > 0) && !C::SPLIT_DQ) {
+          // dP_b goes into the columns dQ_{b-1} occupies until copied out
+          ok = warp_wait(bar_dqfree, par(b + 1), SITE_B_DQFREE);
+          if (!ok) break;
+        }
+        ok = warp_wait(bar_fulldo(st), use_parity(b), SITE_B_FULL);
         if (!ok) break;
-      }
-      ok = warp_wait(bar_fulldo(st), use_parity(i), SITE_B_FULL);
-      if (!ok) break;
-      tc_fence_after();
-      issue_kmajor(C::DP_COL, sV, sdO(st), bar_dp);
-      // dV += P^T dO_i once the gradient warps have written P^T.
-      ok = warp_wait(bar_p, i & 1, SITE_B_P);
-      if (!ok) break;
-      tc_fence_after();
-      if (elect_one()) {
-        const uint64_t dod = sdesc_sw128(sdO(st), BOX, 1024);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + C::DV_COL, tmem + C::S_COL + C::p_col(kk), dod + kk * (2048 >> 4), ID_DV,
-                 (i > 0 || kk > 0) ? 1u : 0u);
-      }
-      __syncwarp();
-      if (C::EARLY_S && i + 1 < n_i) {
-        ok = issue_next_s(i + 1);  // S_{i+1} behind dV_i, which has read P^T_i
+        tc_fence_after();
+        issue_kmajor(C::DP_COL, sV, sdO(st), bar_dp);
+        // dV += P^T dO_b once the gradient warps have written P^T (for the
+        // first block of a unit this also says that they have read the
+        // previous unit's dV and dK out).
+        ok = warp_wait(bar_p, par(b), SITE_B_P);
         if (!ok) break;
-      }
-      // dK += dS^T Q_i and dQ_i = dS K_j once dS^T is in shared memory.
-      ok = warp_wait(bar_ds, i & 1, SITE_B_DS);
-      if (!ok) break;
-      if (C::SPLIT_DQ && i > 0) {
-        // dQ_i goes into the columns of dQ_{i-1}: copied out by now?
-        ok = warp_wait(bar_dqfree, (i - 1) & 1, SITE_B_DQFREE);
-        if (!ok) break;
-      }
-      tc_fence_after();
-      if (elect_one()) {
-        const uint64_t dsk = sdesc_sw128(sDS, 16, 1024);     // dS^T, K-major
-        const uint64_t dsm = sdesc_sw128(sDS, BOX, 1024);    // the same tile, MN-major
-        const uint64_t qmn = sdesc_sw128(sQ(st), BOX, 1024);
-        const uint64_t kmn = sdesc_sw128(sK, BOX, 1024);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + C::DK_COL, dsk + (((kk >> 2) * BOX + (kk & 3) * 32) >> 4),
-                 qmn + kk * (2048 >> 4), ID_DK, (i > 0 || kk > 0) ? 1u : 0u);
-        if constexpr (C::DQ_HALVES) {
-          // columns 64h..64h+63 of dQ_i from box h of K (MN-major, N = 64)
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const uint64_t kh = sdesc_sw128(sK + hh * BOX, BOX, 1024);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ss(tmem + C::DQ_COL + 64 * hh, dsm + kk * (2048 >> 4), kh + kk * (2048 >> 4),
-                     ID_DQH, kk > 0 ? 1u : 0u);
-            mma_commit(hh == 0 ? bar_dq : bar_dq2);
-          }
-        } else {
+        tc_fence_after();
+        if (elect_one()) {
+          const uint64_t dod = sdesc_sw128(sdO(st), BOX, 1024);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tmem + C::DQ_COL, dsm + kk * (2048 >> 4), kmn + kk * (2048 >> 4), ID_DQ,
-                   kk > 0 ? 1u : 0u);
-          mma_commit(bar_dq);
+            mma_ts(tmem + C::DV_COL, tmem + C::S_COL + C::p_col(kk), dod + kk * (2048 >> 4), ID_DV,
+                   (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        __syncwarp();
+        if (C::EARLY_S && i + 1 < n_i) {
+          ok = issue_next_s((b + 1) % BM);  // S_{b+1} behind dV_b, which has read P^T_b
+          if (!ok) break;
+        }
+        // dK += dS^T Q_b and dQ_b = dS K_j once dS^T is in shared memory.
+        ok = warp_wait(bar_ds, par(b), SITE_B_DS);
+        if (!ok) break;
+        if (C::SPLIT_DQ && (k > 0 || i > 0)) {
+          // dQ_b goes into the columns of dQ_{b-1}: copied out by now?
+          ok = warp_wait(bar_dqfree, par(b + 1), SITE_B_DQFREE);
+          if (!ok) break;
+        }
+        tc_fence_after();
+        if (elect_one()) {
+          const uint64_t dsk = sdesc_sw128(sDS, 16, 1024);     // dS^T, K-major
+          const uint64_t dsm = sdesc_sw128(sDS, BOX, 1024);    // the same tile, MN-major
+          const uint64_t qmn = sdesc_sw128(sQ(st), BOX, 1024);
+          const uint64_t kmn = sdesc_sw128(sK, BOX, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + C::DK_COL, dsk + (((kk >> 2) * BOX + (kk & 3) * 32) >> 4),
+                   qmn + kk * (2048 >> 4), ID_DK, (i > 0 || kk > 0) ? 1u : 0u);
+          if constexpr (C::DQ_HALVES) {
+            // columns 64h..64h+63 of dQ_b from box h of K (MN-major, N = 64)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const uint64_t kh = sdesc_sw128(sK + hh * BOX, BOX, 1024);
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                mma_ss(tmem + C::DQ_COL + 64 * hh, dsm + kk * (2048 >> 4), kh + kk * (2048 >> 4),
+                       ID_DQH, kk > 0 ? 1u : 0u);
+              mma_commit(hh == 0 ? bar_dq : bar_dq2);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss(tmem + C::DQ_COL, dsm + kk * (2048 >> 4), kmn + kk * (2048 >> 4), ID_DQ,
+                     kk > 0 ? 1u : 0u);
+            mma_commit(bar_dq);
+          }
+        }
+        __syncwarp();
+        if (!C::EARLY_S && i + 1 < n_i) {
+          ok = issue_next_s((b + 1) % BM);
+          if (!ok) break;
         }
       }
-      __syncwarp();
-      if (!C::EARLY_S && i + 1 < n_i) {
-        ok = issue_next_s(i + 1);
-        if (!ok) break;
-      }
-    }
-    if (ok) {
+      if (!ok) break;
+      // every MMA of the unit: dV_j and dK_j final, K_j and V_j free
       if (elect_one()) mma_commit(bar_fin);
       __syncwarp();
+      g = (g + n_i) % BM;
     }
     if (!ok) {
       // Every MMA already issued must finish before the tensor memory is freed.
@@ -703,38 +852,47 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     }
   } else if (C::DQ_WARPS > 0 && warp >= C::FIRST_DQ_WARP) {
     // ------------------------------------------------------------ dQ warps
-    // Warp q (TMEM lanes 32q..32q+31 = query rows of dQ_i): per block, dQ_i
+    // Warp q (TMEM lanes 32q..32q+31 = query rows of dQ_b): per block, dQ_b
     // out of tensor memory, 32 columns at a time, then into the staging
-    // pieces of the block's Q/dO buffers (every MMA that read Q_i and dO_i is
+    // pieces of the block's Q/dO buffers (every MMA that read Q_b and dO_b is
     // complete: the dq_full arrival follows them).
     const int quarter = warp & 3;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     bool ok = true;
-    for (int i = 0; i < n_i && ok; ++i) {
-      const int st = i % C::STAGES;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_dq, i & 1, ctl, SITE_B_DQ));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t qv[D / 32][32];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_base + C::DQ_COL + 32 * c, qv[c]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) reg_fence32(qv[c]);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_dqfree);
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint8_t* const row_ptr = base_ptr + (dq_box(st, c * 4 + quarter) - base) + lane * 128;
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(row_ptr + ((u ^ (lane & 7)) * 16)) =
-              make_uint4(qv[c][4 * u], qv[c][4 * u + 1], qv[c][4 * u + 2], qv[c][4 * u + 3]);
+    int b = 0;  // modulo BM
+    for (int k = 0; ok; ++k) {
+      int n_i = 0;
+      const int unit = read_unit(k, n_i);
+      if (unit < 0) {
+        ok = unit == -1;
+        break;
       }
-      fence_proxy_async_smem();  // the producer's reduce reads the stage via the async proxy
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_dqst(st));
+      for (int i = 0; i < n_i && ok; ++i, b = (b + 1) % BM) {
+        const int st = stage_of(b);
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_dq, par(b), ctl, SITE_B_DQ));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t qv[D / 32][32];
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_base + C::DQ_COL + 32 * c, qv[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) reg_fence32(qv[c]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_dqfree);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint8_t* const row_ptr = base_ptr + (dq_box(st, c * 4 + quarter) - base) + lane * 128;
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(row_ptr + ((u ^ (lane & 7)) * 16)) =
+                make_uint4(qv[c][4 * u], qv[c][4 * u + 1], qv[c][4 * u + 2], qv[c][4 * u + 3]);
+        }
+        fence_proxy_async_smem();  // the producer's reduce reads the stage via the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_dqst(st));
+      }
     }
   } else {
     // ------------------------------------------------------------ gradient warps
@@ -747,13 +905,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const int key = jblk * 128 + r;
-    const bool key_ok = key < L;
-    const bool tail_blk = (jblk + 1) * 128 > L;  // some key of this block is past L
+    // the current unit
+    Unit w{};
+    int g0 = 0;  // its first block, modulo BM
+    // this lane's key is w.jblk * 128 + r; the unit's block has keys past L
+    // only if it is the last one of a ragged L
+    auto key_ok = [&] { return w.jblk * 128 + r < L; };
+    auto tail_blk = [&] { return (w.jblk + 1) * 128 > L; };
     const uint64_t sl2x2 = f2_pack(args.scale_log2, args.scale_log2);
     const uint64_t scale2 = f2_pack(args.scale, args.scale);
-    auto terms_of = [&](int i) {
-      return reinterpret_cast<const float*>(rowterms(i % C::STAGES)) + CQ * h;
+    auto terms_of = [&](int b) {
+      return reinterpret_cast<const float*>(rowterms(stage_of(b))) + CQ * h;
     };
     float p[CQ];  // P^T of this warp's queries, block of the last phase A
 
@@ -763,12 +925,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     // masks apply only on the causal diagonal block and in the last key
     // block of a ragged L (both uniform across the CTA); elsewhere the
     // per-element selects are compiled out.
-    auto phase_a = [&](int i) -> bool {
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_s, i & 1, ctl, SITE_B_S))) return false;
+    // b: the block modulo BM; i: its index in the unit
+    auto phase_a = [&](int b, int i) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_s, par(b), ctl, SITE_B_S))) return false;
       tc_fence_after();
-      const int qb = q_first + i;
-      const bool diag = CAUSAL && qb == jblk;
-      const float* const terms = terms_of(i);
+      const int qb = w.q_first + i;
+      const bool diag = CAUSAL && qb == w.jblk;
+      const float* const terms = terms_of(b);
       uint32_t sr[CQ];
       bwd_tmem_ld<CQ>(lane_base + C::S_COL + CQ * h, sr);
       tmem_wait_ld();
@@ -793,7 +956,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             // causal: key r > query (CQ*h + e + u) of the same block;
             // keys past L (zero rows of K) never contribute.
             if constexpr (MASK)
-              if ((diag && r > CQ * h + e + u) || !key_ok) pe[u] = 0.f;
+              if ((diag && r > CQ * h + e + u) || !key_ok()) pe[u] = 0.f;
             p[e + u] = pe[u];
           }
           pk[e >> 1] = pack_bf16x2(pe[0], pe[1]);
@@ -801,7 +964,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         }
         bwd_tmem_st<CQ / 2>(lane_base + C::S_COL + CQ * h, pk);
       };
-      if (diag || tail_blk)
+      if (diag || tail_blk())
         compute(std::true_type{});
       else
         compute(std::false_type{});
@@ -815,10 +978,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     // Phase B of block i: dS^T = P^T (.) (scale * dP^T - scale * D), bf16
     // into the 128B-swizzled dS tile: row = key, box b holds queries
     // 64b..64b+63, 16-byte unit u of row r at unit u ^ (r % 8).
-    auto phase_b = [&](int i) -> bool {
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_dp, i & 1, ctl, SITE_B_DP))) return false;
+    auto phase_b = [&](int b) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_dp, par(b), ctl, SITE_B_DP))) return false;
       tc_fence_after();
-      const float* const terms = terms_of(i);
+      const float* const terms = terms_of(b);
       uint32_t dr[CQ];
       bwd_tmem_ld<CQ>(lane_base + C::DP_COL + CQ * h, dr);
       tmem_wait_ld();
@@ -875,13 +1038,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       fence_proxy_async_smem();  // the producer's reduce reads the stage via the async proxy
       __syncwarp();
     };
-    auto phase_c = [&](int i) -> bool {
-      const int st = i % C::STAGES;
+    auto phase_c = [&](int b) -> bool {
+      const int st = stage_of(b);
       if constexpr (C::DQ_HALVES) {
         constexpr int HW = 64 / BWD_GRAD_GROUPS;  // columns per warp and half
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          if (!__all_sync(0xffffffffu, mbar_wait(hh == 0 ? bar_dq : bar_dq2, i & 1, ctl, SITE_B_DQ)))
+          if (!__all_sync(0xffffffffu, mbar_wait(hh == 0 ? bar_dq : bar_dq2, par(b), ctl, SITE_B_DQ)))
             return false;
           tc_fence_after();
           uint32_t qv[HW];
@@ -897,7 +1060,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           if (lane == 0) mbar_arrive(hh == 0 ? bar_dqst(st) : bar_dqst2(st));
         }
       } else {
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_dq, i & 1, ctl, SITE_B_DQ))) return false;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_dq, par(b), ctl, SITE_B_DQ))) return false;
         tc_fence_after();
         uint32_t qv[CW];
         bwd_tmem_ld<CW>(lane_base + C::DQ_COL + CW * h, qv);
@@ -913,35 +1076,48 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     };
 
     bool ok = true;
-    if constexpr (C::EARLY_S) {
-      // A(0); then per block B(i), A(i+1), C(i): P of the next block is
-      // computed while dK_i and dQ_i run on the tensor core.
-      ok = phase_a(0);
-      for (int i = 0; i < n_i && ok; ++i) {
-        ok = phase_b(i);
-        if (ok && i + 1 < n_i) ok = phase_a(i + 1);
-        if (C::DQ_WARPS == 0 && ok) ok = phase_c(i);
+    for (int k = 0; ok; ++k) {
+      int n_i = 0;
+      const int unit = read_unit(k, n_i);
+      if (unit < 0) {
+        ok = unit == -1;
+        break;
       }
-    } else {
-      for (int i = 0; i < n_i && ok; ++i) {
-        ok = phase_a(i);
-        if (ok) ok = phase_b(i);
-        if (ok) ok = phase_c(i);
+      w = decode(unit);
+      if constexpr (C::EARLY_S) {
+        // A(0); then per block B(i), A(i+1), C(i): P of the next block is
+        // computed while dK_i and dQ_i run on the tensor core.
+        ok = phase_a(g0, 0);
+        for (int i = 0; i < w.n_i && ok; ++i) {
+          const int b = (g0 + i) % BM;
+          ok = phase_b(b);
+          if (ok && i + 1 < w.n_i) ok = phase_a((b + 1) % BM, i + 1);
+          if (C::DQ_WARPS == 0 && ok) ok = phase_c(b);
+        }
+      } else {
+        for (int i = 0; i < w.n_i && ok; ++i) {
+          const int b = (g0 + i) % BM;
+          ok = phase_a(b, i);
+          if (ok) ok = phase_b(b);
+          if (ok) ok = phase_c(b);
+        }
       }
-    }
 
-    // Epilogue: dV_j and dK_j are final once every MMA of the CTA has
-    // completed.  With phase C on these warps the last dq_full arrival says
-    // so; when the dQ warps copy dQ out, these warps wait for the MMA warp's
-    // final commit instead (a single phase: they observe none of dq_full's,
-    // and a parity wait on a barrier several phases behind would alias).
-    // bf16 (round to nearest even), rows < L.
-    if (C::DQ_WARPS > 0 && ok) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_fin, 0, ctl, SITE_B_DQ));
-      if (ok) tc_fence_after();
-    }
-    if (ok) {
-      const size_t row = static_cast<size_t>(bh) * L + key;
+      // Epilogue: dV_j and dK_j are final once every MMA of the unit has
+      // completed.  With phase C on these warps the unit's last dq_full
+      // arrival says so; when the dQ warps copy dQ out, these warps wait
+      // for the MMA warp's commit after the unit (fin: one phase per unit;
+      // they observe none of dq_full's, and a parity wait on a barrier
+      // several phases behind would alias).  bf16 (round to nearest even),
+      // rows < L.  The next unit's dV and dK products start only after
+      // these warps' next P-ready arrival, which follows these loads.
+      if (C::DQ_WARPS > 0 && ok) {
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(bar_fin, static_cast<uint32_t>(k) & 1u, ctl, SITE_B_DQ));
+        if (ok) tc_fence_after();
+      }
+      if (!ok) break;
+      const size_t row = static_cast<size_t>(w.bh) * L + w.jblk * 128 + r;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const uint32_t col0 = (which == 0 ? C::DV_COL : C::DK_COL) + CW * h;
@@ -950,7 +1126,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         bwd_tmem_ld<CW>(lane_base + col0, v);
         tmem_wait_ld();
         reg_fence_n(v);
-        if (key_ok) {
+        if (key_ok()) {
           uint4* dst = reinterpret_cast<uint4*>(out + row * D + CW * h);
 #pragma unroll
           for (int u = 0; u < CW / 8; ++u)
@@ -960,6 +1136,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                                 pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7])));
         }
       }
+      g0 = (g0 + w.n_i) % BM;
     }
   }
 

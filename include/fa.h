@@ -245,9 +245,10 @@ int fa_fwd_fp8(const void *q8, const void *k8, const void *v, const float *q_sca
 
 /*
  * fa_bwd_workspace_bytes -- bytes of workspace fa_bwd needs for these sizes:
- * 256-byte-aligned room for an fp32 dQ accumulator [B, H, L, d] and two fp32
- * per-query arrays [B, H, Lp] (Lp = L rounded up to a multiple of 128).
- * Returns 0 for invalid sizes (B/H/L < 1, d not 64/128).  Host only.
+ * 256-byte-aligned room for an fp32 dQ accumulator [B, H, L, d], two fp32
+ * per-query arrays [B, H, Lp] (Lp = L rounded up to a multiple of 128) and
+ * 256 bytes for the gradient kernel's work counter.  Returns 0 for invalid
+ * sizes (B/H/L < 1, d not 64/128).  Host only.
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int L, int d);
 

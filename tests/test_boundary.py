@@ -183,7 +183,8 @@ def test_bwd_workspace_bytes(lib):
     Lp = 384
     acc = ((B * H * L * d * 4 + 255) // 256) * 256
     row = ((B * H * Lp * 4 + 255) // 256) * 256
-    assert fa.fa_bwd_workspace_bytes(B, H, L, d) == acc + 2 * row
+    sched = 256  # the gradient kernel's unit counter
+    assert fa.fa_bwd_workspace_bytes(B, H, L, d) == acc + 2 * row + sched
     assert fa.fa_bwd_workspace_bytes(B, H, L, 96) == 0
     assert fa.fa_bwd_workspace_bytes(0, H, L, d) == 0
     assert fa.fa_bwd_workspace_bytes(B, H, 0, d) == 0
