@@ -83,7 +83,10 @@
 // second.  At d = 128 dQ_i is computed as two 64-column halves with a
 // commit each: the first half is staged, reduced and the Q buffer refilled
 // while the tensor core computes the second, and the Q copy enters the
-// copy engine before the second half's reduce.
+// copy engine before the second half's reduce.  dK_j and dV_j leave at the
+// end of a unit as bf16 from the gradient warps; at d = 128 each warp
+// passes its part through its own bytes of the dS tile first, so that its
+// global stores are row-contiguous.
 #pragma once
 
 #include <cuda.h>
@@ -1117,23 +1120,68 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         if (ok) tc_fence_after();
       }
       if (!ok) break;
-      const size_t row = static_cast<size_t>(w.bh) * L + w.jblk * 128 + r;
-#pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t col0 = (which == 0 ? C::DV_COL : C::DK_COL) + CW * h;
-        uint16_t* const out = which == 0 ? args.dv : args.dk;
-        uint32_t v[CW];
-        bwd_tmem_ld<CW>(lane_base + col0, v);
-        tmem_wait_ld();
-        reg_fence_n(v);
-        if (key_ok()) {
-          uint4* dst = reinterpret_cast<uint4*>(out + row * D + CW * h);
+      if constexpr (D == 128) {
+        // The stores are made row-contiguous through the warp's own bytes of
+        // the dS tile (the bytes it writes in phase B: rows 32*quarter..+31,
+        // 64 bytes each, 128-byte swizzled).  No other warp touches them, no
+        // product reads the tile before the next unit's dS-ready arrivals,
+        // and every product that read it has completed.  Each lane writes its
+        // own row's 64 bytes of dV (then dK); read back, four neighbouring
+        // lanes hold one row's, so a store instruction covers 8 rows in
+        // 64-byte pieces instead of 32 rows in 16-byte pieces (measured: the
+        // 16-byte stores of 16 warps held the epilogue for about 8,000
+        // cycles and delayed the next unit's first product).
+        uint8_t* const mine = ds_ptr + ((CQ * h) >> 6) * BOX + quarter * 32 * 128;
+        const int pu0 = ((CQ * h) & 63) >> 3;  // the warp's first unit in a row
+#pragma unroll 1
+        for (int which = 0; which < 2; ++which) {  // dV, then dK
+          uint32_t v[CW];
+          bwd_tmem_ld<CW>(lane_base + (which == 0 ? C::DV_COL : C::DK_COL) + CW * h, v);
+          tmem_wait_ld();
+          reg_fence_n(v);
 #pragma unroll
           for (int u = 0; u < CW / 8; ++u)
-            dst[u] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * u]), __uint_as_float(v[8 * u + 1])),
-                                pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3])),
-                                pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5])),
-                                pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7])));
+            *reinterpret_cast<uint4*>(mine + lane * 128 + (((pu0 + u) ^ (lane & 7)) * 16)) =
+                make_uint4(pack_bf16x2(__uint_as_float(v[8 * u]), __uint_as_float(v[8 * u + 1])),
+                           pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3])),
+                           pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5])),
+                           pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7])));
+          __syncwarp();
+          uint16_t* const out = which == 0 ? args.dv : args.dk;
+          const int q = lane & 3;  // unit within the row
+#pragma unroll 1
+          for (int s = 0; s < 4; ++s) {
+            const int rr = s * 8 + (lane >> 2);  // row within the warp's 32
+            const uint4 val = *reinterpret_cast<const uint4*>(
+                mine + rr * 128 + (((pu0 + q) ^ (rr & 7)) * 16));
+            const int key = w.jblk * 128 + quarter * 32 + rr;
+            if (key < L)
+              *reinterpret_cast<uint4*>(out + (static_cast<size_t>(w.bh) * L + key) * D + CW * h +
+                                        q * 8) = val;
+          }
+          __syncwarp();
+        }
+      } else {
+        // d = 64: each lane stores its own row's 32 bytes (measured: the
+        // route through the dS tile gained nothing here)
+        const size_t row = static_cast<size_t>(w.bh) * L + w.jblk * 128 + r;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          const uint32_t col0 = (which == 0 ? C::DV_COL : C::DK_COL) + CW * h;
+          uint16_t* const out = which == 0 ? args.dv : args.dk;
+          uint32_t v[CW];
+          bwd_tmem_ld<CW>(lane_base + col0, v);
+          tmem_wait_ld();
+          reg_fence_n(v);
+          if (key_ok()) {
+            uint4* dst = reinterpret_cast<uint4*>(out + row * D + CW * h);
+#pragma unroll
+            for (int u = 0; u < CW / 8; ++u)
+              dst[u] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * u]), __uint_as_float(v[8 * u + 1])),
+                                  pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3])),
+                                  pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5])),
+                                  pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7])));
+          }
         }
       }
       g0 = (g0 + w.n_i) % BM;
