@@ -84,6 +84,37 @@ def test_bwd_many_heads_in_several_scheduling_groups(dev, d, causal):
                  f"B={B} H={H} L={L} d={d} causal={causal}")
 
 
+@pytest.mark.parametrize("delta", [-1, 0, 1])
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_unit_count_around_the_sm_count(dev, delta, d):
+    # The gradient grid is persistent: min(units, SMs) CTAs, the first unit
+    # by CTA index and the rest claimed from a counter.  One unit per head
+    # (L = 100): one unit fewer than the SMs, as many, and one more (the
+    # first claim of some CTA then succeeds and of all others fails).
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    H, L = sms + delta, 100
+    seed = 3700 + delta + d
+    qb, kb, vb = make_custom(1, H, L, d, seed)
+    dob = make_custom_grad_out(1, H, L, d, seed)
+    for causal in (False, True):
+        _full_parity(dev, qb, kb, vb, dob, 1.0 / math.sqrt(d), causal,
+                     f"H={H} L={L} d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_many_units_per_cta(dev, causal):
+    # 2000 heads of L = 64: about 13 one-block units for each CTA, so the
+    # per-block barrier phases, the stage ring and the unit slots run
+    # through many units of one CTA
+    B, H, L, d = 4, 500, 64, 64
+    seed = 3800 + int(causal)
+    qb, kb, vb = make_custom(B, H, L, d, seed)
+    dob = make_custom_grad_out(B, H, L, d, seed)
+    _full_parity(dev, qb, kb, vb, dob, 1.0 / math.sqrt(d), causal,
+                 f"B={B} H={H} L={L} d={d} causal={causal}")
+
+
 @pytest.mark.parametrize("B,H", [(2, 3), (3, 1)])
 @pytest.mark.parametrize("d", [64, 128])
 def test_bwd_batch_heads(dev, B, H, d):
